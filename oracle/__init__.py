@@ -1,0 +1,216 @@
+"""Python access to the CPU oracle of the LLM.int8() decomposed matmul.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg use this package; the product library never
+imports it.  The arithmetic lives in ``llmint8_oracle.c`` (plain C, compiled
+here with gcc on first use); this module only marshals numpy arrays.
+
+Step names follow the method's steps:
+  A0 quantize_weight   per-output-column absmax int8 codes of W
+  A1 outlier_columns   K-columns of X with some |x| > t
+  A2 quantize_rows     per-row absmax int8 codes of the non-outlier part of X
+  A3 int8_matmul       exact integer product of the codes (int64)
+  A4 outlier_matmul    fp16 product of the outlier slice (double)
+  A5 merge             C * s_x * s_w / 127^2 + F, rounded to fp16
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "llmint8_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+          "-pthread", "-Wall"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc if the shared object is missing or stale."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH) or
+             os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int64
+            lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_half_to_double.restype = ctypes.c_double
+            lib.oracle_double_to_half.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_half.restype = ctypes.c_uint16
+            lib.oracle_scale_factor.argtypes = [ctypes.c_float]
+            lib.oracle_scale_factor.restype = ctypes.c_float
+            lib.oracle_code.argtypes = [ctypes.c_float, ctypes.c_float]
+            lib.oracle_code.restype = ctypes.c_int8
+            lib.oracle_quantize_weight.argtypes = [P, I, I, P, P]
+            lib.oracle_outlier_columns.argtypes = [P, I, I, ctypes.c_float, P]
+            lib.oracle_quantize_rows.argtypes = [P, I, I, P, P, P]
+            lib.oracle_int8_matmul.argtypes = [P, P, I, I, I, P, ctypes.c_int]
+            lib.oracle_outlier_matmul.argtypes = [P, P, P, I, I, I, P, ctypes.c_int]
+            lib.oracle_merge.argtypes = [P, P, P, P, I, I, P]
+            for f in ("oracle_quantize_weight", "oracle_outlier_columns", "oracle_quantize_rows",
+                      "oracle_int8_matmul", "oracle_outlier_matmul", "oracle_merge"):
+                getattr(lib, f).restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bits(a) -> np.ndarray:
+    """fp16 array -> contiguous uint16 bit pattern."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        return a.view(np.uint16)
+    if a.dtype == np.uint16:
+        return a
+    raise TypeError(f"expected float16 data, got {a.dtype}")
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+# -- scalar helpers ---------------------------------------------------------------
+
+def half_to_double(bits: int) -> float:
+    return _load().oracle_half_to_double(int(bits))
+
+
+def double_to_half(v: float) -> int:
+    return int(_load().oracle_double_to_half(float(v)))
+
+
+def scale_factor(absmax: float) -> float:
+    return float(_load().oracle_scale_factor(float(absmax)))
+
+
+def code(x: float, sf: float) -> int:
+    return int(_load().oracle_code(float(x), float(sf)))
+
+
+def to_half(values: np.ndarray) -> np.ndarray:
+    """Vector form of double_to_half (returns float16)."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float64).ravel()
+    out = np.fromiter((lib.oracle_double_to_half(float(x)) for x in v), dtype=np.uint16, count=v.size)
+    return out.view(np.float16).reshape(np.shape(values))
+
+
+# -- method steps -------------------------------------------------------------------
+
+def quantize_weight(W: np.ndarray):
+    """A0: W fp16 [K,N] -> (Wq int8 [K,N], s_w float32 [N] = column absmax)."""
+    Wb = _bits(W)
+    K, N = Wb.shape
+    Wq = np.empty((K, N), np.int8)
+    sw = np.empty(N, np.float32)
+    _load().oracle_quantize_weight(_ptr(Wb), K, N, _ptr(Wq), _ptr(sw))
+    return Wq, sw
+
+
+def outlier_columns(X: np.ndarray, t: float) -> np.ndarray:
+    """A1: bool [K], True where some |X[i,j]| > t."""
+    Xb = _bits(X)
+    M, K = Xb.shape
+    out = np.empty(K, np.uint8)
+    _load().oracle_outlier_columns(_ptr(Xb), M, K, float(t), _ptr(out))
+    return out.astype(bool)
+
+
+def quantize_rows(X: np.ndarray, is_outlier: np.ndarray):
+    """A2: (Xq int8 [M,K] with outlier columns zero, s_x float32 [M])."""
+    Xb = _bits(X)
+    M, K = Xb.shape
+    mask = np.ascontiguousarray(is_outlier, dtype=np.uint8)
+    Xq = np.empty((M, K), np.int8)
+    sx = np.empty(M, np.float32)
+    _load().oracle_quantize_rows(_ptr(Xb), M, K, _ptr(mask), _ptr(Xq), _ptr(sx))
+    return Xq, sx
+
+
+def int8_matmul(Xq: np.ndarray, Wq: np.ndarray, nthreads: int | None = None) -> np.ndarray:
+    """A3: exact C = Xq . Wq in int64."""
+    Xq = np.ascontiguousarray(Xq, np.int8)
+    Wq = np.ascontiguousarray(Wq, np.int8)
+    M, K = Xq.shape
+    K2, N = Wq.shape
+    assert K == K2
+    C = np.empty((M, N), np.int64)
+    _load().oracle_int8_matmul(_ptr(Xq), _ptr(Wq), M, K, N, _ptr(C), nthreads or default_threads())
+    return C
+
+
+def outlier_matmul(X: np.ndarray, W: np.ndarray, is_outlier: np.ndarray,
+                   nthreads: int | None = None) -> np.ndarray:
+    """A4: F = X[:, O] . W[O, :] in double."""
+    Xb, Wb = _bits(X), _bits(W)
+    M, K = Xb.shape
+    K2, N = Wb.shape
+    assert K == K2
+    mask = np.ascontiguousarray(is_outlier, dtype=np.uint8)
+    F = np.empty((M, N), np.float64)
+    _load().oracle_outlier_matmul(_ptr(Xb), _ptr(Wb), _ptr(mask), M, K, N, _ptr(F),
+                                  nthreads or default_threads())
+    return F
+
+
+def merge(C: np.ndarray, s_x: np.ndarray, s_w: np.ndarray, F: np.ndarray | None) -> np.ndarray:
+    """A5: Y fp16 = RNE(C * s_x * s_w / 127^2 + F)."""
+    C = np.ascontiguousarray(C, np.int64)
+    M, N = C.shape
+    sx = np.ascontiguousarray(s_x, np.float32)
+    sw = np.ascontiguousarray(s_w, np.float32)
+    Fp = None
+    if F is not None:
+        F = np.ascontiguousarray(F, np.float64)
+        Fp = _ptr(F)
+    Y = np.empty((M, N), np.uint16)
+    _load().oracle_merge(_ptr(C), _ptr(sx), _ptr(sw), Fp, M, N, _ptr(Y))
+    return Y.view(np.float16)
+
+
+def outlier_indices(is_outlier: np.ndarray) -> np.ndarray:
+    """Sorted int32 indices of the outlier columns."""
+    return np.flatnonzero(np.asarray(is_outlier)).astype(np.int32)
+
+
+def llmint8_matmul(X: np.ndarray, W: np.ndarray, t: float, rows=None, nthreads: int | None = None,
+                   wq=None):
+    """The whole path A0..A5 for Y = X.W with threshold t.
+
+    Outlier detection (A1) always scans all rows of X, because the outlier set
+    is a property of the whole activation matrix.  ``rows`` (optional index
+    array) restricts A2..A5 to those rows, for spot checks of large problems.
+    ``wq`` may pass a precomputed (Wq, s_w) from quantize_weight.
+    Returns a dict with every intermediate.
+    """
+    Wq, s_w = wq if wq is not None else quantize_weight(W)
+    is_out = outlier_columns(X, t)
+    Xs = X if rows is None else np.ascontiguousarray(X[np.asarray(rows)])
+    Xq, s_x = quantize_rows(Xs, is_out)
+    C = int8_matmul(Xq, Wq, nthreads)
+    F = outlier_matmul(Xs, W, is_out, nthreads) if is_out.any() else np.zeros(C.shape, np.float64)
+    Y = merge(C, s_x, s_w, F)
+    return dict(Y=Y, C=C, F=F, Xq=Xq, s_x=s_x, Wq=Wq, s_w=s_w, is_outlier=is_out,
+                outliers=outlier_indices(is_out))
