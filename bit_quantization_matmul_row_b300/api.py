@@ -1,0 +1,166 @@
+"""Python binding of the LLM.int8() C ABI, same names as include/llmint8.h.
+
+Argument marshalling only: torch tensors supply device pointers, shapes and the
+current CUDA stream; every step of the computation runs in libllmint8.so.
+Outputs that are not passed in are allocated with torch (device memory is the
+one thing PyTorch is used for).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+
+
+class LLMInt8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {llmint8_status_str(status)} (status {status})")
+
+
+def llmint8_status_str(status: int) -> str:
+    return _lib.load().llmint8_status_str(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != _lib.OK:
+        raise LLMInt8Error(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    if t is None:
+        return
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+def llmint8_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(_lib.load().llmint8_workspace_bytes(int(M), int(K), int(N)))
+
+
+def llmint8_workspace_layout(M: int, K: int, N: int) -> dict:
+    off = (ctypes.c_size_t * len(_lib.WS_FIELDS))()
+    _check(_lib.load().llmint8_workspace_layout(int(M), int(K), int(N), off), "llmint8_workspace_layout")
+    return {name: int(off[i]) for i, name in enumerate(_lib.WS_FIELDS)}
+
+
+def make_workspace(M: int, K: int, N: int, device=None) -> torch.Tensor:
+    n = llmint8_workspace_bytes(M, K, N)
+    if n == 0:
+        raise ValueError(f"unsupported shape M={M} K={K} N={N}")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def llmint8_quantize_weight(W: torch.Tensor, Wq=None, colScaleW=None, Wq16=None, fp16_codes: bool = True,
+                            stream=None):
+    """A0: W fp16 [K, N] -> (Wq int8 [N, K], colScaleW fp32 [N], Wq16 fp16 [N, K] or None)."""
+    K, N = W.shape
+    dev = W.device
+    if Wq is None:
+        Wq = torch.empty((N, K), dtype=torch.int8, device=dev)
+    if colScaleW is None:
+        colScaleW = torch.empty((N,), dtype=torch.float32, device=dev)
+    if Wq16 is None and fp16_codes:
+        Wq16 = torch.empty((N, K), dtype=torch.float16, device=dev)
+    _need(W, torch.float16, (K, N), "W")
+    _need(Wq, torch.int8, (N, K), "Wq")
+    _need(colScaleW, torch.float32, (N,), "colScaleW")
+    _need(Wq16, torch.float16, (N, K), "Wq16")
+    st = _lib.load().llmint8_quantize_weight(_ptr(W), K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Wq16), _stream(stream))
+    _check(st, "llmint8_quantize_weight")
+    return Wq, colScaleW, Wq16
+
+
+def _shapes(X, Wq):
+    M, K = X.shape
+    N = Wq.shape[0]
+    return M, K, N
+
+
+def llmint8_matmul(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspace=None, stream=None):
+    """A1..A5: Y = X.W with the LLM.int8() decomposition at `threshold`."""
+    M, K, N = _shapes(X, Wq)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    if workspace is None:
+        workspace = make_workspace(M, K, N, X.device)
+    _need(X, torch.float16, (M, K), "X")
+    _need(Y, torch.float16, (M, N), "Y")
+    st = _lib.load().llmint8_matmul(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
+                                    _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "llmint8_matmul")
+    return Y
+
+
+def llmint8_matmul_int8(X, Wq, colScaleW, Wq16, Y=None, workspace=None, stream=None):
+    """Plain vector-wise int8 (threshold = +inf, no fp16 weight)."""
+    M, K, N = _shapes(X, Wq)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    if workspace is None:
+        workspace = make_workspace(M, K, N, X.device)
+    _need(X, torch.float16, (M, K), "X")
+    _need(Y, torch.float16, (M, N), "Y")
+    st = _lib.load().llmint8_matmul_int8(_ptr(X), M, K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Wq16), _ptr(Y),
+                                         _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "llmint8_matmul_int8")
+    return Y
+
+
+def llmint8_matmul_i32(X, threshold, Wq, colScaleW, Wq16, C=None, workspace=None, stream=None):
+    """Same path, but returns the exact int32 accumulator C = Xq . Wq^T of step A3."""
+    M, K, N = _shapes(X, Wq)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.int32, device=X.device)
+    if workspace is None:
+        workspace = make_workspace(M, K, N, X.device)
+    _need(X, torch.float16, (M, K), "X")
+    _need(C, torch.int32, (M, N), "C")
+    st = _lib.load().llmint8_matmul_i32(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
+                                        _ptr(C), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "llmint8_matmul_i32")
+    return C
+
+
+def llmint8_device_status(workspace, stream=None) -> int:
+    """Synchronize and read (then clear) the device error word; returns a status code."""
+    return int(_lib.load().llmint8_device_status(_ptr(workspace), _stream(stream)))
+
+
+def llmint8_selftest_timeout(workspace, spin_limit: int, stream=None):
+    _check(_lib.load().llmint8_selftest_timeout(_ptr(workspace), int(spin_limit), _stream(stream)),
+           "llmint8_selftest_timeout")
+
+
+def read_intermediates(workspace: torch.Tensor, M: int, K: int, N: int) -> dict:
+    """Copy the X-pass results of the last call out of a workspace (tests/diagnostics).
+
+    Returns row_scale (fp32 [M]), codes (int8 [M, K], decoded from the stored
+    fp16 values), outliers (sorted int32) and status.
+    """
+    lay = llmint8_workspace_layout(M, K, N)
+    ws = workspace
+    count = int(ws[lay["outlier_count"]:lay["outlier_count"] + 4].view(torch.int32).item())
+    idx = ws[lay["outlier_idx"]:lay["outlier_idx"] + 4 * count].view(torch.int32).clone()
+    row_scale = ws[lay["row_scale"]:lay["row_scale"] + 4 * M].view(torch.float32).clone()
+    codes16 = ws[lay["codes"]:lay["codes"] + 2 * M * K].view(torch.float16).view(M, K)
+    codes = codes16.to(torch.int8)
+    status = int(ws[lay["status"]:lay["status"] + 4].view(torch.int32).item())
+    return dict(row_scale=row_scale, codes=codes, codes_fp16=codes16.clone(), outliers=idx,
+                outlier_count=count, status=status)
+
+
+INF = math.inf

@@ -1,0 +1,383 @@
+// C ABI of the LLM.int8() decomposed matmul (declarations and contracts in
+// include/llmint8.h).  Host side: argument checks, workspace layout, tensor-map
+// encoding and kernel launches.  Every step of the path runs in the kernels of
+// this library; there is no host or library fallback.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "llmint8.h"
+#include "common.cuh"
+#include "xpass.cuh"
+#include "wquant.cuh"
+#include "gemv.cuh"
+#include "gemm_tc.cuh"
+
+using namespace llmint8;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+    bool gemm_attr_set = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+llmint8_status current_device(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LLMINT8_ECUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return LLMINT8_ECUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.probed = true;
+    }
+    if (!d.supported) return LLMINT8_EUNSUPPORTED;
+    *out = &d;
+    return LLMINT8_OK;
+}
+
+llmint8_status get_encoder() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode) return LLMINT8_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return LLMINT8_ECUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return LLMINT8_OK;
+}
+
+// 2D fp16 tensor [rows, cols] row-major with row pitch `pitch` elements; box
+// of box_rows x 64 columns, 128-byte swizzle (the MMA operand layout).
+llmint8_status encode_fp16_2d(CUtensorMap* map, const void* base, int rows, int cols, int pitch, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? LLMINT8_OK : LLMINT8_ECUDA;
+}
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+    size_t hdr, bitmap, idx, row_scale, codes, xo, w16o, total;
+    int kp;  // padded pitch of the gathered outlier operands (multiple of 64)
+    bool decode;
+};
+
+Layout make_layout(int M, int K, int N) {
+    Layout L;
+    L.decode = M <= LLMINT8_DECODE_MAX_M;
+    L.kp = (int)align_up((size_t)K, 64);
+    size_t off = 0;
+    L.hdr = off;
+    off += 256;
+    L.bitmap = off;
+    off = align_up(off + (size_t)((K + 31) / 32) * 4, 256);
+    L.idx = off;
+    off = align_up(off + (size_t)K * 4, 256);
+    L.row_scale = off;
+    off = align_up(off + (size_t)M * 4, 256);
+    L.codes = off;
+    off = align_up(off + (size_t)M * K * 2, 256);
+    L.xo = off;
+    if (!L.decode) off = align_up(off + (size_t)M * L.kp * 2, 256);
+    L.w16o = off;
+    if (!L.decode) off = align_up(off + (size_t)N * L.kp * 2, 256);
+    L.total = off;
+    return L;
+}
+
+bool sizes_ok(int M, int K, int N) { return M >= 1 && K >= 1 && N >= 1 && K <= kMaxK && N <= (1 << 30); }
+
+llmint8_status launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? LLMINT8_OK : LLMINT8_ECUDA;
+}
+
+int row_quant_vpt(int K) {
+    const int nvec = K / 8;
+    if (nvec <= kRowThreads) return 1;
+    if (nvec <= 2 * kRowThreads) return 2;
+    if (nvec <= 4 * kRowThreads) return 4;
+    if (nvec <= 8 * kRowThreads) return 8;
+    return 0;
+}
+
+llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
+                           const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
+                           void* workspace, size_t ws_bytes, void* stream_) {
+    if (!X || !Wq || !colScaleW || !out) return LLMINT8_EINVAL;
+    if (!sizes_ok(M, K, N) || std::isnan(threshold)) return LLMINT8_EINVAL;
+    const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
+    const bool decode = M <= LLMINT8_DECODE_MAX_M;
+    if (use_outliers && !W16 && !write_i32) return LLMINT8_EINVAL;
+    if (!decode && !Wq16) return LLMINT8_EINVAL;
+    if ((K % 16) || (N % 16)) return LLMINT8_EALIGN;
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(colScaleW) || !aligned16(out) ||
+        (Wq16 && !aligned16(Wq16)) || (W16 && !aligned16(W16)) || !aligned16(workspace))
+        return LLMINT8_EALIGN;
+    const Layout L = make_layout(M, K, N);
+    if (!workspace || ws_bytes < L.total) return LLMINT8_EWORKSPACE;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = current_device(&dev);
+    if (st != LLMINT8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream_);
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.hdr);
+    uint32_t* bitmap = reinterpret_cast<uint32_t*>(ws + L.bitmap);
+    int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
+    float* row_scale = reinterpret_cast<float*>(ws + L.row_scale);
+    __half* codes = reinterpret_cast<__half*>(ws + L.codes);
+    __half* xo = reinterpret_cast<__half*>(ws + L.xo);
+    __half* w16o = reinterpret_cast<__half*>(ws + L.w16o);
+    const __half* Xh = static_cast<const __half*>(X);
+
+    // the header (error word, outlier count) and the outlier bit map start at zero:
+    // the error word reports this call
+    if (cudaMemsetAsync(ws + L.hdr, 0, L.idx - L.hdr, s) != cudaSuccess) return LLMINT8_ECUDA;
+
+    // A1: outlier columns
+    if (use_outliers) {
+        const int gx = (K + kScanCols - 1) / kScanCols;
+        int gy = (M + 7) / 8;
+        const int cap = (dev->sms * 8 + gx - 1) / gx;
+        if (gy > cap) gy = cap;
+        if (gy < 1) gy = 1;
+        k_outlier_scan<<<dim3(gx, gy), kScanThreads, 0, s>>>(Xh, M, K, threshold, bitmap);
+        if ((st = launch_status()) != LLMINT8_OK) return st;
+    }
+
+    // A2: row scales and codes (+ gathered outlier columns for the tensor-core path)
+    RowQuantArgs ra;
+    ra.X = Xh;
+    ra.M = M;
+    ra.K = K;
+    ra.bitmap = bitmap;
+    ra.hdr = hdr;
+    ra.outlier_idx = idx;
+    ra.row_scale = row_scale;
+    ra.codes = codes;
+    ra.xo = (!decode && use_outliers) ? xo : nullptr;
+    ra.xo_pitch = L.kp;
+    switch (row_quant_vpt(K)) {
+        case 1: k_row_quant<1><<<M, kRowThreads, 0, s>>>(ra); break;
+        case 2: k_row_quant<2><<<M, kRowThreads, 0, s>>>(ra); break;
+        case 4: k_row_quant<4><<<M, kRowThreads, 0, s>>>(ra); break;
+        case 8: k_row_quant<8><<<M, kRowThreads, 0, s>>>(ra); break;
+        default: k_row_quant<0><<<M, kRowThreads, 0, s>>>(ra); break;
+    }
+    if ((st = launch_status()) != LLMINT8_OK) return st;
+
+    if (decode) {
+        // A3-A5, decode GEMV
+        GemvArgs ga;
+        ga.codes = codes;
+        ga.Wq = Wq;
+        ga.col_scale = colScaleW;
+        ga.row_scale = row_scale;
+        ga.X = Xh;
+        ga.W16 = static_cast<const __half*>(W16);
+        ga.hdr = hdr;
+        ga.outlier_idx = idx;
+        ga.out = out;
+        ga.M = M;
+        ga.K = K;
+        ga.N = N;
+        const int ksteps = (K + 63) / 64;
+        ga.k_per_warp = ((ksteps + kGemvWarps - 1) / kGemvWarps) * 64;
+        ga.use_outliers = use_outliers ? 1 : 0;
+        const dim3 grid(N / kGemvCols);
+        if (M <= 8) {
+            if (write_i32) k_gemv_decode<1, true><<<grid, kGemvWarps * 32, 0, s>>>(ga);
+            else k_gemv_decode<1, false><<<grid, kGemvWarps * 32, 0, s>>>(ga);
+        } else {
+            if (write_i32) k_gemv_decode<2, true><<<grid, kGemvWarps * 32, 0, s>>>(ga);
+            else k_gemv_decode<2, false><<<grid, kGemvWarps * 32, 0, s>>>(ga);
+        }
+        return launch_status();
+    }
+
+    // A4 operand: gathered, transposed outlier rows of W16
+    if (use_outliers && !write_i32) {
+        k_gather_w16_outlier_rows<<<(N + 63) / 64, 256, 0, s>>>(static_cast<const __half*>(W16), N, hdr, idx, w16o,
+                                                                L.kp);
+        if ((st = launch_status()) != LLMINT8_OK) return st;
+    }
+    if ((st = get_encoder()) != LLMINT8_OK) return st;
+    CUtensorMap tm_a, tm_b, tm_xo, tm_wo;
+    if ((st = encode_fp16_2d(&tm_a, codes, M, K, K, kBM)) != LLMINT8_OK) return st;
+    if ((st = encode_fp16_2d(&tm_b, Wq16, N, K, K, kBN)) != LLMINT8_OK) return st;
+    if ((st = encode_fp16_2d(&tm_xo, xo, M, L.kp, L.kp, kBM)) != LLMINT8_OK) return st;
+    if ((st = encode_fp16_2d(&tm_wo, w16o, N, L.kp, L.kp, kBN)) != LLMINT8_OK) return st;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!dev->gemm_attr_set) {
+            if (cudaFuncSetAttribute(k_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kGemmSmem) != cudaSuccess)
+                return LLMINT8_ECUDA;
+            dev->gemm_attr_set = true;
+        }
+    }
+    GemmArgs ga;
+    ga.row_scale = row_scale;
+    ga.col_scale = colScaleW;
+    ga.hdr = hdr;
+    ga.err = hdr;
+    ga.out = out;
+    ga.M = M;
+    ga.N = N;
+    ga.K = K;
+    // the int32 accumulator leaves the outlier slice out (it is not part of C)
+    ga.use_outliers = (use_outliers && !write_i32) ? 1 : 0;
+    ga.spin_limit = kDefaultSpinLimit;
+    const int ntiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+    const int grid = ntiles < dev->sms ? ntiles : dev->sms;
+    if (write_i32)
+        k_gemm_tc<true><<<grid, kGemmThreads, kGemmSmem, s>>>(tm_a, tm_b, tm_xo, tm_wo, ga);
+    else
+        k_gemm_tc<false><<<grid, kGemmThreads, kGemmSmem, s>>>(tm_a, tm_b, tm_xo, tm_wo, ga);
+    return launch_status();
+}
+
+// Waits on a barrier nothing completes, bounded by spin_limit polls, then
+// records the timeout in the error word.
+__global__ void k_selftest_timeout(WsHeader* hdr, uint32_t spin_limit) {
+    __shared__ uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (!mbar_wait_bounded(&bar, 0, spin_limit, &abort_flag)) record_error(hdr, kStatusTimeout, 99);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* llmint8_status_str(int status) {
+    switch (status) {
+        case LLMINT8_OK: return "LLMINT8_OK";
+        case LLMINT8_EINVAL: return "LLMINT8_EINVAL: invalid argument";
+        case LLMINT8_EALIGN: return "LLMINT8_EALIGN: K/N not a multiple of 16 or pointer not 16-byte aligned";
+        case LLMINT8_EWORKSPACE: return "LLMINT8_EWORKSPACE: workspace missing or too small";
+        case LLMINT8_ECUDA: return "LLMINT8_ECUDA: CUDA runtime call or kernel launch failed";
+        case LLMINT8_ETIMEOUT: return "LLMINT8_ETIMEOUT: a bounded device wait gave up";
+        case LLMINT8_EUNSUPPORTED: return "LLMINT8_EUNSUPPORTED: device is not sm_103";
+        default: return "LLMINT8: unknown status";
+    }
+}
+
+llmint8_status llmint8_quantize_weight(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* Wq16,
+                                       void* stream) {
+    if (!W || !Wq || !colScaleW) return LLMINT8_EINVAL;
+    if (K < 1 || N < 1 || K > (1 << 30) || N > (1 << 30)) return LLMINT8_EINVAL;
+    if ((K % 16) || (N % 16)) return LLMINT8_EALIGN;
+    if (!aligned16(W) || !aligned16(Wq) || !aligned16(colScaleW) || (Wq16 && !aligned16(Wq16))) return LLMINT8_EALIGN;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = current_device(&dev);
+    if (st != LLMINT8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(colScaleW, 0, (size_t)N * 4, s) != cudaSuccess) return LLMINT8_ECUDA;
+    const int gx = (N + 255) / 256;
+    int gy = (K + 7) / 8;
+    const int cap = (dev->sms * 8 + gx - 1) / gx;
+    if (gy > cap) gy = cap;
+    if (gy < 1) gy = 1;
+    k_col_absmax<<<dim3(gx, gy), 256, 0, s>>>(static_cast<const __half*>(W), K, N, colScaleW);
+    if ((st = launch_status()) != LLMINT8_OK) return st;
+    k_quantize_weight_tile<<<dim3((N + 63) / 64, (K + 63) / 64), 256, 0, s>>>(
+        static_cast<const __half*>(W), K, N, colScaleW, Wq, static_cast<__half*>(Wq16));
+    return launch_status();
+}
+
+size_t llmint8_workspace_bytes(int M, int K, int N) {
+    if (!sizes_ok(M, K, N)) return 0;
+    return make_layout(M, K, N).total;
+}
+
+llmint8_status llmint8_matmul(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
+                              const float* colScaleW, const void* Wq16, const void* W16, void* Y, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, workspace_bytes,
+                       stream);
+}
+
+llmint8_status llmint8_matmul_int8(const void* X, int M, int K, int N, const int8_t* Wq, const float* colScaleW,
+                                   const void* Wq16, void* Y, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    return matmul_impl(X, M, K, N, INFINITY, Wq, colScaleW, Wq16, nullptr, Y, false, workspace, workspace_bytes,
+                       stream);
+}
+
+llmint8_status llmint8_matmul_i32(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
+                                  const float* colScaleW, const void* Wq16, int32_t* C, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, nullptr, C, true, workspace, workspace_bytes,
+                       stream);
+}
+
+llmint8_status llmint8_workspace_layout(int M, int K, int N, size_t* offsets) {
+    if (!offsets || !sizes_ok(M, K, N)) return LLMINT8_EINVAL;
+    const Layout L = make_layout(M, K, N);
+    offsets[LLMINT8_WS_STATUS] = L.hdr + offsetof(WsHeader, status);
+    offsets[LLMINT8_WS_OUTLIER_COUNT] = L.hdr + offsetof(WsHeader, outlier_count);
+    offsets[LLMINT8_WS_OUTLIER_IDX] = L.idx;
+    offsets[LLMINT8_WS_ROW_SCALE] = L.row_scale;
+    offsets[LLMINT8_WS_CODES] = L.codes;
+    return LLMINT8_OK;
+}
+
+llmint8_status llmint8_device_status(void* workspace, void* stream) {
+    if (!workspace) return LLMINT8_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LLMINT8_ECUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return LLMINT8_ECUDA;
+    if (word != 0 && cudaMemset(workspace, 0, 4) != cudaSuccess) return LLMINT8_ECUDA;
+    return static_cast<llmint8_status>(word);
+}
+
+llmint8_status llmint8_selftest_timeout(void* workspace, int spin_limit, void* stream) {
+    if (!workspace || spin_limit < 1 || spin_limit > 10000000) return LLMINT8_EINVAL;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = current_device(&dev);
+    if (st != LLMINT8_OK) return st;
+    k_selftest_timeout<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<WsHeader*>(workspace),
+                                                                        (uint32_t)spin_limit);
+    return launch_status();
+}
+
+}  // extern "C"

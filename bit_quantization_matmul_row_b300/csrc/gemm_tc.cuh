@@ -1,0 +1,318 @@
+// Prefill path (M > 16) of the LLM.int8() matmul: steps A3-A5 on the 5th-
+// generation tensor cores.
+//
+// sm_103a has no int8 tcgen05 MMA (kind::i8 exists only on sm_100a/sm_110a),
+// and its int8 mma.sync rate is ~140 TOPS.  The int8 codes are therefore fed to
+// tcgen05.mma kind::f16 as exact fp16 integers.  Each product is an integer of
+// magnitude <= 127^2 = 16129 and each partial sum over at most 1024 products
+// stays below 2^24, so the fp32 TMEM accumulator holds it exactly.  The K loop
+// is cut into chunks of 1024 (16 steps of 64); each chunk is accumulated into
+// one of two TMEM buffers and the epilogue warps drain it into int32 registers
+// while the tensor core fills the other buffer.  The integer product C is thus
+// exact for any K (A3).
+//
+// The fp16 outlier slice (A4: X[:, O] . W16[O, :], fp32 accumulate) is one more
+// chunk of the same pipeline, fed from the gathered operands Xo [M, Kp] and
+// W16oT [N, Kp]; it stays in fp32.  The epilogue then computes
+// Y = fp16(C * s_x[i] * s_w[n] / 127^2 + F) and stores it (A5).
+//
+// Roles (320 threads, one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      TMA producer: 4-stage ring of (A 128x64, B 256x64) fp16 tiles
+//   warp 1      TMEM owner and MMA issuer (one thread), M=128 N=256 K=16 MMAs
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).., column half (w-2)/4
+#pragma once
+
+#include "common.cuh"
+
+namespace llmint8 {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kStages = 4;
+constexpr int kChunkSteps = 16;  // 16 x 64 = 1024 products per exact fp32 chunk
+constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 64 + kEpiWarps * 32;
+constexpr uint32_t kStageA = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kStageB = kBN * kBK * 2;  // 32 KB
+constexpr uint32_t kTmemCols = 512;          // two 256-column fp32 accumulators
+constexpr size_t kGemmSmem = 1024 /*align slack*/ + (size_t)kStages * (kStageA + kStageB) + 256;
+
+struct GemmArgs {
+    const float* row_scale;  // [M]
+    const float* col_scale;  // [N]
+    const WsHeader* hdr;     // outlier_count
+    WsHeader* err;           // error word
+    void* out;               // Y fp16 [M, N] or C int32 [M, N]
+    int M, N, K;
+    int use_outliers;
+    uint32_t spin_limit;
+};
+
+struct GemmSmem {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t teardown;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+};
+
+template <bool WRITE_I32>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+              const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_wo, GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stage_a = smem;
+    uint8_t* stage_b = smem + kStages * kStageA;
+    GemmSmem* ss = reinterpret_cast<GemmSmem*>(smem + kStages * (kStageA + kStageB));
+    volatile uint32_t* abort_flag = &ss->abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_m = (a.M + kBM - 1) / kBM, tiles_n = (a.N + kBN - 1) / kBN;
+    const int ntiles = tiles_m * tiles_n;
+    const int ksteps = (a.K + kBK - 1) / kBK;
+    const int nchunks_int = (ksteps + kChunkSteps - 1) / kChunkSteps;
+    const int n_out = a.use_outliers ? a.hdr->outlier_count : 0;
+    const int osteps = (n_out + kBK - 1) / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ss->full[s], 1);
+            mbar_init(&ss->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ss->tmem_full[b], 1);
+            mbar_init(&ss->tmem_empty[b], kEpiWarps);
+        }
+        mbar_init(&ss->teardown, 1);
+        ss->abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        if (osteps) {
+            tma_prefetch_desc(&tm_xo);
+            tma_prefetch_desc(&tm_wo);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(&ss->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ss->tmem_base;
+
+    auto fail = [&](uint32_t where) {
+        *abort_flag = 1u;
+        record_error(a.err, kStatusTimeout, where);
+    };
+    // whole-warp bounded wait: lane 0 polls, the verdict is broadcast, and the
+    // warp is converged again for the .sync.aligned TMEM loads that follow
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        uint32_t got = 0;
+        if (lane == 0) got = mbar_wait_bounded(bar, parity, a.spin_limit, abort_flag) ? 1u : 0u;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        return got != 0;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_parity[kStages];
+            bool issued[kStages];
+            for (int s = 0; s < kStages; ++s) issued[s] = false, issued_parity[s] = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const int tm = tile % tiles_m, tn = tile / tiles_m;
+                const int total = ksteps + osteps;
+                for (int s = 0; s < total; ++s) {
+                    if (!mbar_wait_bounded(&ss->empty[stage], phase ^ 1u, a.spin_limit, abort_flag)) {
+                        fail(1);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&ss->full[stage], kStageA + kStageB);
+                    if (s < ksteps) {
+                        tma_load_2d(stage_a + stage * kStageA, &tm_a, &ss->full[stage], s * kBK, tm * kBM);
+                        tma_load_2d(stage_b + stage * kStageB, &tm_b, &ss->full[stage], s * kBK, tn * kBN);
+                    } else {
+                        const int so = s - ksteps;
+                        tma_load_2d(stage_a + stage * kStageA, &tm_xo, &ss->full[stage], so * kBK, tm * kBM);
+                        tma_load_2d(stage_b + stage * kStageB, &tm_wo, &ss->full[stage], so * kBK, tn * kBN);
+                    }
+                    issued[stage] = true;
+                    issued_parity[stage] = phase;
+                    if (++stage == kStages) stage = 0, phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                // let copies already in flight land before the CTA can exit
+                for (int s = 0; s < kStages; ++s)
+                    if (issued[s]) mbar_wait_bounded(&ss->full[s], issued_parity[s], 1u << 20, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc_f16(kBM, kBN);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t chunk = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const int nchunks = nchunks_int + (osteps ? 1 : 0);
+                for (int ch = 0; ch < nchunks && ok; ++ch, ++chunk) {
+                    const uint32_t b = chunk & 1u, use = (chunk >> 1) & 1u;
+                    if (!mbar_wait_bounded(&ss->tmem_empty[b], use ^ 1u, a.spin_limit, abort_flag)) {
+                        fail(2);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int s_begin = ch < nchunks_int ? ch * kChunkSteps : ksteps;
+                    const int s_end = ch < nchunks_int ? min(ksteps, s_begin + kChunkSteps) : ksteps + osteps;
+                    const uint32_t d_tmem = tmem_base + b * (uint32_t)kBN;
+                    for (int s = s_begin; s < s_end; ++s) {
+                        if (!mbar_wait_bounded(&ss->full[stage], phase, a.spin_limit, abort_flag)) {
+                            fail(3);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t ad = make_sdesc_k128(smem_u32(stage_a + stage * kStageA));
+                        const uint64_t bd = make_sdesc_k128(smem_u32(stage_b + stage * kStageB));
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            // advance 16 fp16 = 32 bytes inside the 128-byte swizzled row
+                            tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                                       (s > s_begin || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(&ss->empty[stage]);
+                        if (++stage == kStages) stage = 0, phase ^= 1u;
+                    }
+                    if (ok) tc_commit(&ss->tmem_full[b]);
+                }
+            }
+            // all issued MMAs complete before TMEM can be released
+            tc_commit(&ss->teardown);
+            mbar_wait_bounded(&ss->teardown, 0, a.spin_limit, nullptr);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;
+        const int q = warp & 3;          // TMEM lane quarter this warp may access
+        const int h = ew >> 2;           // column half of the 256-wide tile
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        uint32_t chunk = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const int tm = tile % tiles_m, tn = tile / tiles_m;
+            const int row = tm * kBM + q * 32 + lane;
+            const int col0 = tn * kBN + h * 128;
+            int32_t sum[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) sum[c] = 0;
+            for (int ch = 0; ch < nchunks_int; ++ch, ++chunk) {
+                const uint32_t b = chunk & 1u, use = (chunk >> 1) & 1u;
+                const bool got = warp_wait(&ss->tmem_full[b], use);
+                if (!got) {
+                    if (lane == 0) fail(4);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(tmem_base + lane_base + b * kBN + h * 128 + j * 16, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) sum[j * 16 + c] += __float2int_rn(__uint_as_float(r[c]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ss->tmem_empty[b]);
+            }
+            if (!ok) break;
+            uint32_t fb = 0;
+            const bool has_f = osteps > 0;
+            if (has_f) {
+                fb = chunk & 1u;
+                const uint32_t use = (chunk >> 1) & 1u;
+                if (!warp_wait(&ss->tmem_full[fb], use)) {
+                    if (lane == 0) fail(5);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            const bool row_ok = row < a.M;
+            const float sx = row_ok ? a.row_scale[row] * (1.0f / 16129.0f) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint32_t r[16];
+                if (has_f) {
+                    tmem_ld_32x32b_x16(tmem_base + lane_base + fb * kBN + h * 128 + j * 16, r);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) r[c] = 0u;
+                }
+                const int cb = col0 + j * 16;
+                if (row_ok) {
+                    if (WRITE_I32) {
+                        int32_t* orow = reinterpret_cast<int32_t*>(a.out) + (size_t)row * a.N;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (cb + v * 4 < a.N)
+                                *reinterpret_cast<int4*>(orow + cb + v * 4) =
+                                    make_int4(sum[j * 16 + v * 4], sum[j * 16 + v * 4 + 1], sum[j * 16 + v * 4 + 2],
+                                              sum[j * 16 + v * 4 + 3]);
+                    } else {
+                        __half* orow = reinterpret_cast<__half*>(a.out) + (size_t)row * a.N;
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            const int c8 = cb + v * 8;
+                            if (c8 < a.N) {
+                                const float4 s0 = __ldg(reinterpret_cast<const float4*>(a.col_scale + c8));
+                                const float4 s1 = __ldg(reinterpret_cast<const float4*>(a.col_scale + c8 + 4));
+                                const float sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                                uint32_t o[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int c = v * 8 + 2 * e;
+                                    const float y0 = fmaf((float)sum[j * 16 + c], sx * sw[2 * e], __uint_as_float(r[c]));
+                                    const float y1 =
+                                        fmaf((float)sum[j * 16 + c + 1], sx * sw[2 * e + 1], __uint_as_float(r[c + 1]));
+                                    __half2 hv = __floats2half2_rn(y0, y1);
+                                    o[e] = *reinterpret_cast<uint32_t*>(&hv);
+                                }
+                                *reinterpret_cast<uint4*>(orow + c8) = make_uint4(o[0], o[1], o[2], o[3]);
+                            }
+                        }
+                    }
+                }
+            }
+            if (has_f) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ss->tmem_empty[fb]);
+                ++chunk;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace llmint8

@@ -1,0 +1,96 @@
+// A0: weight quantization, once per weight matrix (paper walkthrough, section
+// 2.1: one scale per output column of W; Lightning Fabric 8-bit page, section
+// 2.2: per output channel).  The column absmax covers all K rows.
+//
+//   colScaleW[n] = max_k |W[k,n]|
+//   Wq[n, k]     = round-half-away(fp32(W[k,n] * fp32(127 / colScaleW[n])))
+//   Wq16[n, k]   = the same code as an exact fp16 value (tensor-core operand)
+//
+// W is [K, N] row-major; the outputs are transposed to [N, K] (K contiguous):
+// the layout both GEMM paths stream.
+#pragma once
+
+#include "common.cuh"
+
+namespace llmint8 {
+
+// Column absmax, pass 1: each CTA reduces a 256-column strip over a slice of
+// rows and folds its result into colScaleW with an integer atomicMax (valid for
+// non-negative floats).  colScaleW must be zero on entry.
+__global__ void __launch_bounds__(256) k_col_absmax(const __half* __restrict__ W, int K, int N,
+                                                    float* __restrict__ col_amax) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c0 = blockIdx.x * 256 + lane * 8;
+    float m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (c0 < N) {
+        for (int r = blockIdx.y * 8 + warp; r < K; r += gridDim.y * 8) {
+            const uint4 v = ldg_nc_v4(W + (size_t)r * N + c0);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                m[2 * e] = fmaxf(m[2 * e], fabsf(f.x));
+                m[2 * e + 1] = fmaxf(m[2 * e + 1], fabsf(f.y));
+            }
+        }
+    }
+    __shared__ float s[8][256];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s[warp][lane * 8 + e] = m[e];
+    __syncthreads();
+    const int c = blockIdx.x * 256 + threadIdx.x;
+    float r = s[0][threadIdx.x];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) r = fmaxf(r, s[w][threadIdx.x]);
+    if (c < N && r > 0.0f) atomicMax(reinterpret_cast<int*>(col_amax) + c, __float_as_int(r));
+}
+
+// Pass 2: quantize a 64(k) x 64(n) tile and write it transposed.
+__global__ void __launch_bounds__(256) k_quantize_weight_tile(const __half* __restrict__ W, int K, int N,
+                                                              const float* __restrict__ col_amax,
+                                                              int8_t* __restrict__ Wq, __half* __restrict__ Wq16) {
+    __shared__ float s_sf[64];
+    __shared__ int8_t tile[64][64 + 4];  // [n][k]
+    const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    const int tid = threadIdx.x;
+    if (tid < 64) {
+        const int n = n0 + tid;
+        const float amax = n < N ? col_amax[n] : 0.0f;
+        s_sf[tid] = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    }
+    __syncthreads();
+    // read: 64 rows (k) x 64 columns (n), 2 columns per thread-iteration
+    for (int e = tid; e < 64 * 32; e += 256) {
+        const int kr = e >> 5, nc = (e & 31) * 2;
+        const int k = k0 + kr, n = n0 + nc;
+        if (k < K && n < N) {  // N % 16 == 0: n and n+1 both valid
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(W + (size_t)k * N + n));
+            const float q0 = fminf(fmaxf(roundf(__fmul_rn(f.x, s_sf[nc])), -127.0f), 127.0f);
+            const float q1 = fminf(fmaxf(roundf(__fmul_rn(f.y, s_sf[nc + 1])), -127.0f), 127.0f);
+            tile[nc][kr] = (int8_t)(int)q0;
+            tile[nc + 1][kr] = (int8_t)(int)q1;
+        }
+    }
+    __syncthreads();
+    // write: row n, 64 consecutive k; 4 codes per thread-iteration
+    for (int e = tid; e < 64 * 16; e += 256) {
+        const int nr = e >> 4, kc = (e & 15) * 4;
+        const int n = n0 + nr, k = k0 + kc;
+        if (n < N && k < K) {  // K % 16 == 0: all 4 valid
+            const int8_t c0 = tile[nr][kc], c1 = tile[nr][kc + 1], c2 = tile[nr][kc + 2], c3 = tile[nr][kc + 3];
+            const uint32_t packed = (uint32_t)(uint8_t)c0 | ((uint32_t)(uint8_t)c1 << 8) |
+                                    ((uint32_t)(uint8_t)c2 << 16) | ((uint32_t)(uint8_t)c3 << 24);
+            *reinterpret_cast<uint32_t*>(Wq + (size_t)n * K + k) = packed;
+            if (Wq16) {
+                const __half2 h01 = __floats2half2_rn((float)c0, (float)c1);
+                const __half2 h23 = __floats2half2_rn((float)c2, (float)c3);
+                uint2 o;
+                o.x = *reinterpret_cast<const uint32_t*>(&h01);
+                o.y = *reinterpret_cast<const uint32_t*>(&h23);
+                *reinterpret_cast<uint2*>(Wq16 + (size_t)n * K + k) = o;
+            }
+        }
+    }
+}
+
+}  // namespace llmint8

@@ -1,0 +1,276 @@
+// X pass of the LLM.int8() matmul: outlier-column detection (A1) and per-row
+// absmax quantization of the non-outlier columns (A2).
+//
+//   A1 (paper walkthrough, section 2.3): column j of X is an outlier dimension
+//      when some |X[i,j]| exceeds the threshold.
+//   A2 (paper walkthrough, sections 2.1 and 2.3; pitfalls guide, section 1):
+//      s_x[i] = max over non-outlier j of |X[i,j]|,
+//      q = round-half-away(fp32(x * fp32(127 / s_x[i]))), outlier columns -> 0.
+//
+// The outlier set depends on every row and each row's scale depends on the
+// set, so the pass is two kernels: a scan that ORs per-column flags into a bit
+// map (atomics only for words that hold an outlier, which is rare), then one
+// CTA per row that re-reads its row (from L2 when X fits there) and writes the
+// codes.  Codes are written as fp16 values (exact integers in [-127, 127]) --
+// the operand format of both GEMM paths on sm_103a, which has no int8 tcgen05.
+#pragma once
+
+#include "common.cuh"
+
+namespace llmint8 {
+
+constexpr int kScanThreads = 256;
+constexpr int kScanCols = 256;  // columns per CTA: 32 lanes x 8 fp16
+
+// |x| > t for the 8 fp16 values of a 16-byte vector -> 8-bit mask (bit e = element e).
+__device__ __forceinline__ uint32_t outlier_mask8(uint4 v, float t) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        m |= (fabsf(f.x) > t ? 1u : 0u) << (2 * e);
+        m |= (fabsf(f.y) > t ? 1u : 0u) << (2 * e + 1);
+    }
+    return m;
+}
+
+// A1.  grid = (ceil(K/256), row groups); bitmap must be zero on entry.
+__global__ void __launch_bounds__(kScanThreads) k_outlier_scan(const __half* __restrict__ X, int M, int K, float t,
+                                                               uint32_t* __restrict__ bitmap) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c0 = blockIdx.x * kScanCols + lane * 8;
+    uint32_t m = 0;
+    if (c0 < K) {
+        const __half* p = X + c0;
+        int r = blockIdx.y * 8 + warp;
+        const int step = gridDim.y * 8;
+        // two independent loads in flight per iteration
+        for (; r + step < M; r += 2 * step) {
+            const uint4 a = ldg_nc_v4(p + (size_t)r * K);
+            const uint4 b = ldg_nc_v4(p + (size_t)(r + step) * K);
+            m |= outlier_mask8(a, t) | outlier_mask8(b, t);
+        }
+        if (r < M) m |= outlier_mask8(ldg_nc_v4(p + (size_t)r * K), t);
+    }
+    // lanes 4w..4w+3 hold the 32 columns of bitmap word w of this strip
+    uint32_t word = m << (8 * (lane & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    __shared__ uint32_t s_words[8][8];
+    if ((lane & 3) == 0) s_words[warp][lane >> 2] = word;
+    __syncthreads();
+    if (threadIdx.x < 8) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) acc |= s_words[w][threadIdx.x];
+        const int gw = blockIdx.x * (kScanCols / 32) + threadIdx.x;
+        if (acc != 0u && gw < (K + 31) / 32) atomicOr(&bitmap[gw], acc);
+    }
+}
+
+constexpr int kRowThreads = 256;
+constexpr int kMaxK = 65536;             // bitmap words held in shared memory: <= 2048
+constexpr int kMaxWords = kMaxK / 32;
+
+struct RowQuantArgs {
+    const __half* X;
+    int M, K;
+    const uint32_t* bitmap;   // [ceil(K/32)]
+    WsHeader* hdr;            // outlier_count written by block 0
+    int32_t* outlier_idx;     // [K], written by block 0
+    float* row_scale;         // [M]
+    __half* codes;            // [M, K]
+    __half* xo;               // [M, xo_pitch] gathered outlier columns (nullptr: skip)
+    int xo_pitch;             // elements; gathered columns are zero-padded up to a multiple of 64
+};
+
+// Round half away from zero, then clamp to [-127, 127] (clamp after rounding,
+// before the integer conversion: LLM quantization in practice, section 3.2).
+__device__ __forceinline__ float code_of(float x, float sf) {
+    float r = roundf(__fmul_rn(x, sf));
+    return fminf(fmaxf(r, -127.0f), 127.0f);
+}
+
+// A2.  One CTA per row.  VPT = 16-byte vectors per thread kept in registers
+// between the absmax pass and the code pass (the row is re-read when K is
+// larger than 256 * 8 * VPT).
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
+    __shared__ uint32_t s_bits[kMaxWords];
+    __shared__ int32_t s_prefix[kMaxWords];  // outliers in words before w
+    __shared__ int32_t s_wsum[kRowThreads / 32];
+    __shared__ float s_wmax[kRowThreads / 32];
+    __shared__ int32_t s_total;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row = blockIdx.x;
+    const int K = a.K;
+    const int nwords = (K + 31) >> 5;
+
+    // --- bitmap -> shared memory, exclusive prefix of popcounts (block scan) ---
+    constexpr int WPT = kMaxWords / kRowThreads;  // words per thread (8)
+    int local[WPT];
+    int tsum = 0;
+#pragma unroll
+    for (int i = 0; i < WPT; ++i) {
+        const int w = tid * WPT + i;
+        const uint32_t b = (w < nwords) ? a.bitmap[w] : 0u;
+        if (w < nwords) s_bits[w] = b;
+        local[i] = __popc(b);
+        tsum += local[i];
+    }
+    int incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int w = 0; w < kRowThreads / 32; ++w) {
+            const int v = s_wsum[w];
+            s_wsum[w] = run;
+            run += v;
+        }
+        s_total = run;
+    }
+    __syncthreads();
+    int run = s_wsum[warp] + incl - tsum;
+#pragma unroll
+    for (int i = 0; i < WPT; ++i) {
+        const int w = tid * WPT + i;
+        if (w < nwords) s_prefix[w] = run;
+        run += local[i];
+    }
+    __syncthreads();
+    const int n_out = s_total;
+
+    // --- masked absmax over the non-outlier columns of this row ---
+    const __half* xrow = a.X + (size_t)row * K;
+    const int nvec = K >> 3;  // K % 16 == 0
+    uint4 v[VPT > 0 ? VPT : 1];
+    float amax = 0.0f;
+    auto absmax_vec = [&](uint4 x, int c) {
+        const uint32_t om = (s_bits[c >> 5] >> (c & 31)) & 0xFFu;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+            if (!((om >> (2 * e)) & 1u)) amax = fmaxf(amax, fabsf(f.x));
+            if (!((om >> (2 * e + 1)) & 1u)) amax = fmaxf(amax, fabsf(f.y));
+        }
+    };
+    if (VPT > 0) {
+#pragma unroll
+        for (int i = 0; i < (VPT > 0 ? VPT : 1); ++i) {
+            const int vi = tid + i * kRowThreads;
+            if (vi < nvec) v[i] = ldg_nc_v4(xrow + (size_t)vi * 8);
+        }
+#pragma unroll
+        for (int i = 0; i < (VPT > 0 ? VPT : 1); ++i) {
+            const int vi = tid + i * kRowThreads;
+            if (vi < nvec) absmax_vec(v[i], vi * 8);
+        }
+    } else {
+        for (int vi = tid; vi < nvec; vi += kRowThreads) absmax_vec(ldg_nc_v4(xrow + (size_t)vi * 8), vi * 8);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) s_wmax[warp] = amax;
+    __syncthreads();
+    amax = s_wmax[0];
+#pragma unroll
+    for (int w = 1; w < kRowThreads / 32; ++w) amax = fmaxf(amax, s_wmax[w]);
+
+    // scale factor 127 / absmax in fp32, correctly rounded; absmax 0 -> 0
+    const float sf = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+
+    // --- codes (outlier columns -> 0) ---
+    __half* crow = a.codes + (size_t)row * K;
+    auto code_vec = [&](uint4 x, int c) {
+        const uint32_t om = (s_bits[c >> 5] >> (c & 31)) & 0xFFu;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+            const float q0 = ((om >> (2 * e)) & 1u) ? 0.0f : code_of(f.x, sf);
+            const float q1 = ((om >> (2 * e + 1)) & 1u) ? 0.0f : code_of(f.y, sf);
+            __half2 h = __floats2half2_rn(q0, q1);
+            o[e] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(crow + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    if (VPT > 0) {
+#pragma unroll
+        for (int i = 0; i < (VPT > 0 ? VPT : 1); ++i) {
+            const int vi = tid + i * kRowThreads;
+            if (vi < nvec) code_vec(v[i], vi * 8);
+        }
+    } else {
+        for (int vi = tid; vi < nvec; vi += kRowThreads) code_vec(ldg_nc_v4(xrow + (size_t)vi * 8), vi * 8);
+    }
+    if (tid == 0) a.row_scale[row] = amax;
+
+    // --- outlier list (block 0) and gathered outlier columns of this row ---
+    if (n_out > 0 && (a.xo != nullptr || row == 0)) {
+        __half* xo_row = a.xo ? a.xo + (size_t)row * a.xo_pitch : nullptr;
+        for (int w = tid; w < nwords; w += kRowThreads) {
+            uint32_t b = s_bits[w];
+            int pos = s_prefix[w];
+            while (b) {
+                const int bit = __ffs(b) - 1;
+                b &= b - 1;
+                const int col = w * 32 + bit;
+                if (xo_row) xo_row[pos] = xrow[col];
+                if (row == 0) a.outlier_idx[pos] = col;
+                ++pos;
+            }
+        }
+    }
+    if (a.xo != nullptr) {
+        // zero padding up to the next multiple of 64 gathered columns
+        __half* xo_row = a.xo + (size_t)row * a.xo_pitch;
+        const int padded = (n_out + 63) & ~63;
+        for (int c = n_out + tid; c < padded; c += kRowThreads) xo_row[c] = __ushort_as_half(0);
+    }
+    if (row == 0 && tid == 0) a.hdr->outlier_count = n_out;
+}
+
+// A4 operand preparation for the tensor-core GEMM: W16oT[n, p] = W16[O[p], n]
+// for p < count, zero for count <= p < roundup(count, 64).  W16 is [K, N]
+// row-major; the result is [N, pitch] with the gathered K contiguous, the
+// K-major layout the MMA reads.  grid.x = ceil(N / 64); 256 threads.
+__global__ void __launch_bounds__(256) k_gather_w16_outlier_rows(const __half* __restrict__ W16, int N,
+                                                                 const WsHeader* __restrict__ hdr,
+                                                                 const int32_t* __restrict__ outlier_idx,
+                                                                 __half* __restrict__ w16oT, int pitch) {
+    __shared__ __half tile[64][64 + 8];
+    const int count = hdr->outlier_count;
+    const int padded = (count + 63) & ~63;
+    const int n0 = blockIdx.x * 64;
+    const int tid = threadIdx.x;
+    for (int p0 = 0; p0 < padded; p0 += 64) {
+        // load 64 gathered rows x 64 columns (coalesced along n)
+        for (int e = tid; e < 64 * 64; e += 256) {
+            const int pr = e >> 6, nc = e & 63;
+            const int p = p0 + pr, n = n0 + nc;
+            __half v = __ushort_as_half(0);
+            if (p < count && n < N) v = W16[(size_t)outlier_idx[p] * N + n];
+            tile[pr][nc] = v;
+        }
+        __syncthreads();
+        // write transposed: row n, columns p0..p0+63 (coalesced along p)
+        for (int e = tid; e < 64 * 64; e += 256) {
+            const int nr = e >> 6, pc = e & 63;
+            const int n = n0 + nr;
+            if (n < N) w16oT[(size_t)n * pitch + p0 + pc] = tile[pc][nr];
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace llmint8

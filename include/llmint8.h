@@ -1,0 +1,175 @@
+/*
+ * llmint8.h -- C ABI of the LLM.int8() mixed-precision decomposed matmul on one
+ * NVIDIA B300 (sm_103a).
+ *
+ * The operation (Y = X.W, decomposed):
+ *   A0  weights get one absmax scale per output column and int8 codes
+ *       q = round(w * 127/absmax)            ("LLM.int8() paper walkthrough",
+ *       section 2.1; "LLM.int8() quantization pitfalls guide", section 1)
+ *   A1  a K-column of X holding any |x| > threshold is an outlier dimension
+ *       (paper walkthrough, section 2.3; default threshold 6.0)
+ *   A2  the other columns of X get one absmax scale per row and int8 codes;
+ *       outlier columns get code 0            (paper walkthrough, 2.1 and 2.3)
+ *   A3  C = Xq . Wq, exact integer accumulation
+ *   A4  F = X[:, outliers] . W[outliers, :] in fp16 with fp32 accumulation
+ *       (paper walkthrough, 2.3; pitfalls guide, 3.2)
+ *   A5  Y = fp16( C * rowScaleX[i] * colScaleW[n] / 127^2 + F )
+ *       (pitfalls guide, 3.3: dequantize the 8-bit result, then add)
+ *
+ * Code rule: scale_factor = fp32(127 / absmax); q = round-half-away-from-zero(
+ * fp32(x * scale_factor)), clamped to [-127, 127]; absmax 0 gives code 0.
+ * Scales are stored as the absmax values themselves (fp32).
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers to caller-owned memory; the library
+ *     allocates nothing and keeps no pointer after the call returns.
+ *   - fp16 arrays are IEEE binary16, passed as void*.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). All work is
+ *     enqueued asynchronously on it; the call returns without synchronizing.
+ *   - Argument errors are detected on the host before anything is enqueued and
+ *     leave all buffers untouched.  LLMINT8_ECUDA means a CUDA runtime call or a
+ *     kernel launch failed; work enqueued before the failure may have run.
+ *   - Sizes: 1 <= M, 1 <= K <= 65536, 1 <= N (else LLMINT8_EINVAL; M = 0 is
+ *     an empty problem and is rejected, not silently accepted); K and N must be
+ *     multiples of 16 and all pointers 16-byte aligned (else LLMINT8_EALIGN).
+ *   - Inputs must be finite; NaN or Inf inputs give unspecified codes and Y.
+ *   - The device must be compute capability 10.3 (else LLMINT8_EUNSUPPORTED).
+ */
+#ifndef LLMINT8_H
+#define LLMINT8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LLMINT8_OK = 0,
+    LLMINT8_EINVAL = 1,       /* bad size, NULL pointer, NaN threshold, missing operand */
+    LLMINT8_EALIGN = 2,       /* K or N not a multiple of 16, or a pointer not 16-byte aligned */
+    LLMINT8_EWORKSPACE = 3,   /* workspace NULL or smaller than llmint8_workspace_bytes() */
+    LLMINT8_ECUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    LLMINT8_ETIMEOUT = 5,     /* a bounded device-side wait gave up (see llmint8_device_status) */
+    LLMINT8_EUNSUPPORTED = 6  /* current device is not sm_103 */
+} llmint8_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *llmint8_status_str(int status);
+
+/* Largest M served by the decode (GEMV) path; larger M uses the tensor-core GEMM. */
+#define LLMINT8_DECODE_MAX_M 16
+
+/*
+ * A0 -- quantize a weight matrix once, before any forward call.
+ *
+ *   W         in   fp16 [K, N] row-major (the retained fp16 weight; keep it: its
+ *                  rows are gathered for outlier columns of X)
+ *   Wq        out  int8 [N, K] row-major, i.e. K contiguous per output column:
+ *                  Wq[n*K + k] = round-half-away(W[k,n] * fp32(127 / colScaleW[n]))
+ *   colScaleW out  fp32 [N], colScaleW[n] = max_k |W[k, n]| over ALL K rows
+ *   Wq16      out  optional (may be NULL): fp16 [N, K], the same codes as fp16
+ *                  values (exact), the operand layout of the tensor-core GEMM.
+ *                  Required by llmint8_matmul* when M > LLMINT8_DECODE_MAX_M.
+ *
+ * Source: paper walkthrough, section 2.1 (per-column weight scale); Lightning
+ * Fabric 8-bit page, section 2.2 (one scale per output channel).
+ */
+llmint8_status llmint8_quantize_weight(const void *W, int K, int N, int8_t *Wq, float *colScaleW,
+                                       void *Wq16, void *stream);
+
+/* Bytes of device workspace llmint8_matmul* needs for this shape (16-byte multiple). */
+size_t llmint8_workspace_bytes(int M, int K, int N);
+
+/*
+ * A1..A5 -- Y = X.W, LLM.int8() decomposition with the given outlier threshold.
+ *
+ *   X          in   fp16 [M, K] row-major activations
+ *   threshold  in   outlier test |x| > threshold (strict).  +INFINITY disables
+ *                   the decomposition (pure vector-wise int8); 0 or a negative
+ *                   value makes every nonzero column an outlier; NaN -> EINVAL.
+ *   Wq, colScaleW   from llmint8_quantize_weight
+ *   Wq16       in   fp16 codes from llmint8_quantize_weight; may be NULL only if
+ *                   M <= LLMINT8_DECODE_MAX_M
+ *   W16        in   the retained fp16 W [K, N]; may be NULL only if threshold is
+ *                   +INFINITY
+ *   Y          out  fp16 [M, N] row-major
+ *   workspace  scratch device memory of at least llmint8_workspace_bytes(M,K,N)
+ *              bytes; its contents on entry do not matter.  Two calls that share
+ *              a workspace must be ordered (same stream or synchronized).
+ *
+ * Source: paper walkthrough, sections 2.1-2.3; pitfalls guide, sections 3.1-3.3.
+ */
+llmint8_status llmint8_matmul(const void *X, int M, int K, int N, float threshold,
+                              const int8_t *Wq, const float *colScaleW, const void *Wq16,
+                              const void *W16, void *Y, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
+ * Plain vector-wise int8 variant: llmint8_matmul with threshold = +INFINITY and
+ * no fp16 weight.  Row scales run over all K columns; Y = fp16(C * sx * sw / 127^2).
+ * Source: pitfalls guide, section 1 (plain absmax int8, no outlier handling).
+ */
+llmint8_status llmint8_matmul_int8(const void *X, int M, int K, int N, const int8_t *Wq,
+                                   const float *colScaleW, const void *Wq16, void *Y,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* ----------------------------------------------------------------------------
+ * Introspection (tests and diagnostics; not on the hot path)
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Same arguments and kernels as llmint8_matmul, but the GEMM epilogue writes
+ * the exact integer accumulator of step A3 instead of Y:
+ *   C  out  int32 [M, N] row-major, C[i,n] = sum_k Xq[i,k] * Wq[n,k]
+ * (|C| <= K * 127^2 < 2^31 for every accepted K <= 65536).  The fp16 outlier
+ * product is not part of C; threshold still decides which columns of X are
+ * zeroed, and W16 is not needed.
+ */
+llmint8_status llmint8_matmul_i32(const void *X, int M, int K, int N, float threshold,
+                                  const int8_t *Wq, const float *colScaleW, const void *Wq16,
+                                  int32_t *C, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/* Workspace fields whose offsets llmint8_workspace_layout reports. */
+enum {
+    LLMINT8_WS_STATUS = 0,       /* uint32: device error word (0 = OK, else an llmint8_status) */
+    LLMINT8_WS_OUTLIER_COUNT = 1,/* int32: number of outlier columns found by the last call */
+    LLMINT8_WS_OUTLIER_IDX = 2,  /* int32 [count]: outlier column indices, ascending */
+    LLMINT8_WS_ROW_SCALE = 3,    /* fp32 [M]: rowScaleX (absmax over non-outlier columns) */
+    LLMINT8_WS_CODES = 4,        /* fp16 [M, K] row-major: the int8 codes of X stored as
+                                    exact fp16 values (the tensor-core operand format) */
+    LLMINT8_WS_NFIELDS = 5
+};
+
+/*
+ * Byte offsets of the fields above inside a workspace used by a call with the
+ * same (M, K, N).  After a llmint8_matmul* call has completed, the fields hold
+ * that call's intermediate results.  offsets must hold LLMINT8_WS_NFIELDS values.
+ */
+llmint8_status llmint8_workspace_layout(int M, int K, int N, size_t *offsets);
+
+/*
+ * Synchronize `stream`, then read and clear the device error word of `workspace`.
+ * Every llmint8_matmul* call clears the word when it starts, so it reports the
+ * last call that used this workspace (or the last llmint8_selftest_timeout).
+ * Returns LLMINT8_OK, or the status a kernel recorded (LLMINT8_ETIMEOUT when a
+ * bounded wait gave up), or LLMINT8_ECUDA if synchronization itself failed.
+ */
+llmint8_status llmint8_device_status(void *workspace, void *stream);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one small kernel that waits
+ * on a shared-memory barrier that nothing ever completes, giving up after
+ * `spin_limit` polls (1 .. 1e7).  It then records LLMINT8_ETIMEOUT in the
+ * workspace error word and returns; no GPU hang, trap or fault is involved.
+ * The workspace needs at least 256 bytes.
+ */
+llmint8_status llmint8_selftest_timeout(void *workspace, int spin_limit, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLMINT8_H */

@@ -1,0 +1,113 @@
+"""The C-ABI library loads and exports every entry point include/llmint8.h
+declares; host-side argument checks return their documented status before any
+device work (no GPU needed)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from bit_quantization_matmul_row_b300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "llmint8.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(llmint8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and nothing from torch crosses the boundary: plain C symbols
+    out = os.popen(f"nm -D --defined-only {_lib.LIB_PATH}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}\b", out), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.llmint8_status_str(code).decode().startswith("LLMINT8")
+    assert b"unknown" in lib.llmint8_status_str(99)
+
+
+def test_workspace_bytes(lib):
+    assert lib.llmint8_workspace_bytes(0, 64, 64) == 0
+    assert lib.llmint8_workspace_bytes(16, 70000, 64) == 0
+    small = lib.llmint8_workspace_bytes(16, 4096, 4096)
+    big = lib.llmint8_workspace_bytes(2048, 4096, 4096)
+    assert small > 0 and small % 16 == 0
+    # prefill adds the gathered outlier operands: M*Kp + N*Kp fp16
+    assert big >= 2048 * 4096 * 2 * 2 + 4096 * 4096 * 2
+
+
+def test_workspace_layout(lib):
+    off = (ctypes.c_size_t * 5)()
+    assert lib.llmint8_workspace_layout(300, 1088, 400, off) == _lib.OK
+    vals = list(off)
+    assert vals[0] == 0 and vals[1] == 4
+    assert vals[2] < vals[3] < vals[4]
+    assert all(v % 4 == 0 for v in vals)
+    assert vals[4] + 300 * 1088 * 2 <= lib.llmint8_workspace_bytes(300, 1088, 400)
+    assert lib.llmint8_workspace_layout(0, 16, 16, off) == _lib.EINVAL
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails its checks first
+
+
+def _mm(lib, M=32, K=64, N=64, t=6.0, X=FAKE, Wq=FAKE, sw=FAKE, wq16=FAKE, w16=FAKE, Y=FAKE, ws=FAKE, wsb=None):
+    if wsb is None:
+        wsb = 1 << 40
+    P = ctypes.c_void_p
+    return lib.llmint8_matmul(P(X), M, K, N, t, P(Wq), P(sw), P(wq16), P(w16), P(Y), P(ws), wsb, None)
+
+
+def test_matmul_argument_errors(lib):
+    assert _mm(lib, M=0) == _lib.EINVAL
+    assert _mm(lib, K=0) == _lib.EINVAL
+    assert _mm(lib, N=-16) == _lib.EINVAL
+    assert _mm(lib, t=math.nan) == _lib.EINVAL
+    assert _mm(lib, X=0) == _lib.EINVAL
+    assert _mm(lib, w16=0) == _lib.EINVAL            # finite threshold needs W16
+    assert _mm(lib, wq16=0) == _lib.EINVAL           # M > 16 needs the fp16 codes
+    assert _mm(lib, K=72) == _lib.EALIGN
+    assert _mm(lib, N=40) == _lib.EALIGN
+    assert _mm(lib, X=FAKE + 8) == _lib.EALIGN
+    assert _mm(lib, ws=0) == _lib.EWORKSPACE
+    assert _mm(lib, wsb=16) == _lib.EWORKSPACE
+
+
+def test_int8_variant_needs_no_w16(lib):
+    P = ctypes.c_void_p
+    # argument checks pass up to the workspace check: W16 is not required
+    st = lib.llmint8_matmul_int8(P(FAKE), 32, 64, 64, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 16, None)
+    assert st == _lib.EWORKSPACE
+
+
+def test_quantize_weight_argument_errors(lib):
+    P = ctypes.c_void_p
+    assert lib.llmint8_quantize_weight(P(0), 64, 64, P(FAKE), P(FAKE), None, None) == _lib.EINVAL
+    assert lib.llmint8_quantize_weight(P(FAKE), 0, 64, P(FAKE), P(FAKE), None, None) == _lib.EINVAL
+    assert lib.llmint8_quantize_weight(P(FAKE), 65, 64, P(FAKE), P(FAKE), None, None) == _lib.EALIGN
+    assert lib.llmint8_quantize_weight(P(FAKE), 64, 64, P(FAKE + 4), P(FAKE), None, None) == _lib.EALIGN
+
+
+def test_selftest_argument_errors(lib):
+    P = ctypes.c_void_p
+    assert lib.llmint8_selftest_timeout(P(0), 10, None) == _lib.EINVAL
+    assert lib.llmint8_selftest_timeout(P(FAKE), 0, None) == _lib.EINVAL
+    assert lib.llmint8_selftest_timeout(P(FAKE), 10 ** 8, None) == _lib.EINVAL

@@ -1,0 +1,175 @@
+"""CUDA path vs the CPU oracle, element by element (needs a B300).
+
+Sizes span several tiles and ragged tails of both kernels: the decode GEMV
+(M <= 16, 16-column CTAs, K split over 8 warps, exact int32 every 1024 K) and
+the tensor-core GEMM (128 x 256 tiles, 64-wide K steps, 1024-long exact
+chunks, the outlier slice as a final fp32 chunk).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from bit_quantization_matmul_row_b300 import api, synthetic
+from parity import check, run_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.init()
+
+
+def xw(M, K, N, frac=0.01, seed=0, sigma=0.02, mag=(20.0, 60.0), min_count=0):
+    X, _ = synthetic.make_x(M, K, frac=frac, min_count=min_count, mag=mag, seed=seed)
+    W, _ = synthetic.make_w(K, N, sigma=sigma, seed=seed)
+    return X, W
+
+
+# ------------------------------------------------------------------ small, full compare
+
+def test_tiny_config():
+    case = synthetic.tiny()[0]
+    X, planted = case.x()
+    W, _ = case.w()
+    g, ref = check(X, W, case.threshold)
+    assert set(planted.tolist()) <= set(g["outliers"].tolist())
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+def test_decode_ragged(M):
+    # K = 1040: 17 steps of 64 split over 8 warps (ragged last warp, last step 16 wide)
+    X, W = xw(M, 1040, 144, frac=0.01, seed=10 + M, min_count=3)
+    check(X, W, 6.0)
+
+
+@pytest.mark.parametrize("M,K,N", [(17, 64, 256), (130, 272, 272), (300, 1088, 400), (256, 2112, 512)])
+def test_prefill_ragged(M, K, N):
+    # ragged M tiles, ragged N tiles (N % 256 != 0), K not a multiple of 64,
+    # K crossing the 1024-long exact chunk boundary
+    X, W = xw(M, K, N, frac=0.02, seed=M + K + N, min_count=2)
+    check(X, W, 6.0)
+
+
+@pytest.mark.parametrize("M", [4, 200])
+def test_int8_variant(M):
+    X, W = xw(M, 1088, 272, frac=0.02, seed=30 + M)
+    check(X, W, math.inf, int8_variant=True)
+    # t = +inf through the general entry point is the same computation
+    check(X, W, math.inf)
+
+
+@pytest.mark.parametrize("M", [5, 150])
+def test_threshold_zero_all_outliers(M):
+    # every nonzero column is an outlier: the int8 part is empty and the fp16
+    # slice covers all of K (many 64-wide outlier steps on the GEMM path)
+    X, W = xw(M, 1088, 272, frac=0.0, seed=40 + M)
+    X[:, 7] = 0
+    g, ref = check(X, W, 0.0)
+    assert len(g["outliers"]) == 1087
+    assert not g["codes"].any() and not g["C"].any()
+
+
+@pytest.mark.parametrize("M", [2, 140])
+def test_negative_threshold(M):
+    X, W = xw(M, 256, 256, frac=0.0, seed=50 + M)
+    X[:, 3] = 0
+    g, ref = check(X, W, -1.0)
+    assert len(g["outliers"]) == 256
+    assert not g["s_x"].any()
+
+
+@pytest.mark.parametrize("M", [16, 256])
+def test_exactness_beyond_fp32_integer_range(M):
+    # All codes +-127 and K = 8192: |C| reaches 127^2 * 8192 = 132,124,672 > 2^24,
+    # so any accumulation in plain fp32 beyond 1024 products would round.
+    K, N = 8192, 256
+    rng = np.random.default_rng(M)
+    X = np.ones((M, K), np.float16)
+    X[1::2, K // 2:] = -1            # odd rows change sign halfway
+    W = np.full((K, N), 0.02, np.float16)
+    W[:, 1::3] = -0.02
+    signs = rng.choice([-1.0, 1.0], size=(K, 8)).astype(np.float16)
+    W[:, -8:] = signs * np.float16(0.02)  # random signs: large cancellations
+    g, ref = check(X, W, 6.0)
+    assert np.abs(g["C"]).max() == 127 * 127 * K
+
+
+def test_zero_rows_and_columns():
+    X, W = xw(40, 512, 256, frac=0.01, seed=60)
+    X[3] = 0
+    W[:, 5] = 0
+    g, ref = check(X, W, 6.0)
+    assert g["s_x"][3] == 0 and g["s_w"][5] == 0
+    assert not g["Y"][:, 5].any()
+
+
+@pytest.mark.parametrize("M", [7, 129])
+def test_workspace_contents_do_not_matter(M):
+    X, W = xw(M, 512, 256, seed=70 + M)
+    a = run_gpu(X, W, 6.0, want_i32=False)
+    b = run_gpu(X, W, 6.0, want_i32=False, garbage_workspace=True)
+    assert np.array_equal(a["Y"].view(np.uint16), b["Y"].view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [16, 300])
+def test_deterministic_and_stream(M):
+    X, W = xw(M, 1088, 400, seed=80 + M)
+    a = run_gpu(X, W, 6.0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = run_gpu(X, W, 6.0, stream=s)
+    s.synchronize()
+    for k in ("Y", "C", "codes", "s_x"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_bounded_wait_reports_timeout():
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    api.llmint8_selftest_timeout(ws, 1000)
+    assert api.llmint8_device_status(ws) == 5  # LLMINT8_ETIMEOUT, read and cleared
+    assert api.llmint8_device_status(ws) == 0
+    # the context is still usable afterwards
+    X, W = xw(16, 256, 256, seed=90)
+    check(X, W, 6.0)
+
+
+# ------------------------------------------------------------------ full-size workloads
+# Quantization outputs compared in full; C and Y on sampled rows (the oracle
+# computes those rows one by one).  Same entry points and launch configuration
+# as the benchmark.
+
+def _full_case(case, nrows=24):
+    X, planted = case.x()
+    W, _ = case.w()
+    rows = sample_rows(case.M, nrows, seed=case.seed)
+    g, ref = check(X, W, case.threshold, rows=rows)
+    assert set(planted.tolist()) <= set(g["outliers"].tolist())
+
+
+@pytest.mark.parametrize("case", synthetic.decode_7b(), ids=lambda c: c.name)
+def test_decode_7b(case):
+    _full_case(case)
+
+
+@pytest.mark.parametrize("case", synthetic.prefill_7b(), ids=lambda c: c.name)
+def test_prefill_7b(case):
+    _full_case(case)
+
+
+@pytest.mark.parametrize("case", synthetic.ffn_13b(), ids=lambda c: c.name)
+def test_ffn_13b(case):
+    _full_case(case, nrows=16)
+
+
+SWEEP = [c for c in synthetic.sweep_70b()
+         if (c.N == 28672 and c.frac in (0.0, 0.001, 0.05)) or (c.N == 8192 and c.frac == 0.01)]
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=lambda c: c.name)
+def test_sweep_70b(case):
+    _full_case(case, nrows=12)
