@@ -1,0 +1,549 @@
+#!/usr/bin/env python
+"""Benchmark of the LLM.int8() decomposed matmul on B300.
+
+Headline workload (one "step"): the 7B-like decode calls
+  M in {1, 4, 16} x (K, N) in {(4096, 4096), (4096, 11008), (11008, 4096)},
+X ~ N(0,1) fp16 with 0.1 % (at least 4) outlier columns, W ~ N(0, 0.02) fp16,
+threshold 6.0 -- nine llmint8_matmul calls per step.  Metric: GB/s of
+algorithmic bytes (Wq K*N + colScaleW 4N + outlier rows of W 2*n_o*N + X 2MK +
+Y 2MN per call), against the measured HBM copy bandwidth.  Weights are held in
+R replicas that rotate, so every weight matrix is evicted from L2 (126 MB)
+before it is read again.
+
+Also reported in the same JSON line: the 7B-like prefill calls (TOPS of the
+whole call and of the GEMM stage against the measured dense fp16/bf16 peak),
+the end-to-end number through host buffers, the CPU oracle baseline, SM clocks
+sampled during the timed region, and the launch count.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from bit_quantization_matmul_row_b300 import synthetic  # noqa: E402
+
+METRIC = "LLM.int8() matmul TOPS (prefill) & GB/s (decode) vs 1×B300 roofline"
+WORKLOAD = ("7B-like decode: M in {1,4,16} x (K,N) in {(4096,4096),(4096,11008),(11008,4096)}; "
+            "X ~N(0,1) fp16 with 0.1% (>=4) outlier columns of absmax U(20,60); W ~N(0,0.02) fp16; threshold 6.0")
+FALLBACK_HBM = 6400.0
+FALLBACK_BF16 = 1800.0
+L2_BYTES = 126 * 2 ** 20
+
+
+def alg_bytes(M, K, N, n_o):
+    """Algorithmic bytes of one call: int8 weights, column scales, fp16 outlier rows of W, X, Y."""
+    return K * N + 4 * N + 2 * n_o * N + 2 * M * K + 2 * M * N
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)),
+                "measured")
+    except Exception:
+        return FALLBACK_HBM, FALLBACK_BF16, 1400.0, "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms={period_ms}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [s for s in self.samples if t0 - 0.06 <= s[0] <= t1 + 0.06]
+        note = None
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:2]
+            note = "timed region shorter than the sampling period; nearest samples"
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = set()
+        for s in inside:
+            for name, flag in zip(names, s[3][1:]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+               "reasons": sorted(reasons), "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ---------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_time(cases_xw, n_sample_cols=None, min_seconds=10.0, max_reps=8):
+    """Time the CPU oracle (A1..A5 per call, weights quantized beforehand) on the
+    decode calls; optionally on the first n_sample_cols output columns only.
+    Returns (bytes, seconds, reps, threads)."""
+    import oracle
+    oracle.build()
+    prepared = []
+    for (M, K, N, X, W) in cases_xw:
+        Ws = W if n_sample_cols is None else np.ascontiguousarray(W[:, :n_sample_cols])
+        prepared.append((M, K, Ws.shape[1], X, Ws, oracle.quantize_weight(Ws)))
+    threads = oracle.default_threads()
+    total_b, total_t, reps = 0, 0.0, 0
+    while reps < max_reps and (total_t < min_seconds or reps == 0):
+        for (M, K, N, X, Ws, wq) in prepared:
+            t = time.perf_counter()
+            r = oracle.llmint8_matmul(X, Ws, 6.0, wq=wq, nthreads=threads)
+            total_t += time.perf_counter() - t
+            total_b += alg_bytes(M, K, N, int(r["outliers"].size))
+        reps += 1
+    return total_b, total_t, reps, threads
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    cases = synthetic.decode_7b()
+    data = []
+    for c in cases:
+        X, _ = c.x()
+        W, _ = c.w()
+        data.append((c.M, c.K, c.N, X, W))
+    sample_cols = 512
+    import oracle
+    oracle.build()
+    prepared = []
+    for (M, K, N, X, W) in data:
+        Ws = np.ascontiguousarray(W[:, :sample_cols])
+        prepared.append((M, K, X, Ws, oracle.quantize_weight(Ws)))
+    threads = oracle.default_threads()
+
+    def step():
+        b = 0
+        for (M, K, X, Ws, wq) in prepared:
+            r = oracle.llmint8_matmul(X, Ws, 6.0, wq=wq, nthreads=threads)
+            b += alg_bytes(M, K, Ws.shape[1], int(r["outliers"].size))
+        return b
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    b = 0
+    for _ in range(args.steps):
+        b += step()
+    dt = time.perf_counter() - t
+    value = b / dt / 1e9
+    sample = (f"each step: the 9 decode calls (A1..A5 on the CPU oracle, weights pre-quantized) restricted "
+              f"to the first {sample_cols} output columns")
+    line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / max(args.steps, 1) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "calls_per_step": 9, "sample_cols": sample_cols},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def traffic_record(kernel_file):
+    """Per-launch DRAM bytes from the committed ncu summary, valid only while the
+    kernel source is unchanged (hash match); else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "bit_quantization_matmul_row_b300", "csrc", kernel_file)
+    try:
+        d = json.load(open(p))
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        rec = d.get(kernel_file)
+        if rec and rec.get("source_sha256_16") == h:
+            return rec
+    except Exception:
+        pass
+    return None
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+    from bit_quantization_matmul_row_b300 import api
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs (resident in HBM), weights in R rotating replicas
+    R = args.replicas
+    cases = []
+    for c in synthetic.decode_7b():
+        X, _ = c.x()
+        W, _ = c.w()
+        Xd = torch.from_numpy(X).to(dev)
+        Wd = torch.from_numpy(W).to(dev)
+        Wq, sw, _ = api.llmint8_quantize_weight(Wd, fp16_codes=False)
+        reps = [(Wq, sw, Wd)] + [(Wq.clone(), sw.clone(), Wd.clone()) for _ in range(R - 1)]
+        ws = api.make_workspace(c.M, c.K, c.N, dev)
+        Y = torch.empty((c.M, c.N), dtype=torch.float16, device=dev)
+        cases.append(dict(c=c, X=X, Xd=Xd, reps=reps, ws=ws, Y=Y, W=W))
+    torch.cuda.synchronize()
+    # realised outlier counts (deterministic for these inputs) -> algorithmic bytes
+    for d in cases:
+        c = d["c"]
+        api.llmint8_matmul(d["Xd"], c.threshold, *d["reps"][0][:2], None, d["reps"][0][2], Y=d["Y"], workspace=d["ws"])
+    torch.cuda.synchronize()
+    step_bytes = 0
+    for d in cases:
+        c = d["c"]
+        d["n_o"] = api.read_intermediates(d["ws"], c.M, c.K, c.N)["outlier_count"]
+        d["bytes"] = alg_bytes(c.M, c.K, c.N, d["n_o"])
+        step_bytes += d["bytes"]
+    weight_set = sum(d["c"].K * d["c"].N for d in cases[:3])  # distinct (K,N) weights, one replica
+
+    ncase = len(cases)
+
+    # ---- one CUDA graph per step (the 9 llmint8_matmul calls), so the GPU is not
+    # starved by host launch latency.  Inside a call the kernels overlap through
+    # programmatic dependent launch; nothing is inserted between them here.
+    def capture(gi, instrumented):
+        g = torch.cuda.CUDAGraph()
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(ncase)] if instrumented else None
+        with torch.cuda.graph(g):
+            for ci, d in enumerate(cases):
+                c = d["c"]
+                Wq, sw, Wd = d["reps"][(gi * ncase + ci) % R]
+                if instrumented:  # xpass, [event], GEMM stage, [event]
+                    api.llmint8_xpass(d["Xd"], c.threshold, c.N, d["ws"])
+                    evs[ci][0].record()
+                    api.llmint8_gemm(d["Xd"], c.threshold, Wq, sw, None, Wd, d["Y"], d["ws"])
+                    evs[ci][1].record()
+                else:
+                    api.llmint8_matmul(d["Xd"], c.threshold, Wq, sw, None, Wd, Y=d["Y"], workspace=d["ws"])
+        return g, evs
+
+    G = min(args.steps, args.max_graphs)
+    graphs = [capture(gi, False) for gi in range(G)]
+    torch.cuda.synchronize()
+    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    for i in range(args.warmup):
+        graphs[i % G][0].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev_a.record(stream)
+    for i in range(args.steps):
+        graphs[i % G][0].replay()
+    ev_b.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = ev_a.elapsed_time(ev_b)
+    del graphs
+    # dominant kernel: the same steps with event nodes around every GEMM stage
+    # (this separates the GEMV from the X pass, so it runs without their overlap)
+    G = min(args.steps, args.max_graphs, 64)
+    igraphs = [capture(gi, True) for gi in range(G)]
+    for i in range(args.warmup):
+        igraphs[i % G][0].replay()
+    torch.cuda.synchronize()
+    for i in range(G):
+        igraphs[i][0].replay()
+    torch.cuda.synchronize()
+    gemv_ms = [[e0.elapsed_time(e1) for (e0, e1) in igraphs[gi][1]] for gi in range(G)]
+    del igraphs
+    st = api.llmint8_device_status(cases[0]["ws"])
+    if st != 0:
+        raise SystemExit(f"device error word {st}")
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    total_bytes = step_bytes * args.steps * world
+    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+    gemv_total_ms = sum(sum(r) for r in gemv_ms)
+    gemv_launches = G * ncase
+    achieved = step_bytes * G / (gemv_total_ms * 1e-3) / 1e9
+    per_shape = [{"M": d["c"].M, "K": d["c"].K, "N": d["c"].N, "outliers": d["n_o"],
+                  "gemv_us": 1e3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G,
+                  "gemv_gbs": d["bytes"] / (1e-3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G) / 1e9}
+                 for ci, d in enumerate(cases)]
+    time.sleep(0.1)
+
+    # ---- end to end through the public call: pinned host X -> device,
+    # llmint8_matmul, Y -> pinned host; eager (each call from Python) and as a graph
+    hX = [torch.from_numpy(d["X"]).pin_memory() for d in cases]
+    hY = [torch.empty((d["c"].M, d["c"].N), dtype=torch.float16).pin_memory() for d in cases]
+    h2d = sum(d["X"].nbytes for d in cases)
+    d2h = sum(d["c"].M * d["c"].N * 2 for d in cases)
+
+    def e2e_step(i):
+        for ci, d in enumerate(cases):
+            c = d["c"]
+            Wq, sw, Wd = d["reps"][(i * ncase + ci) % R]
+            d["Xd"].copy_(hX[ci], non_blocking=True)
+            api.llmint8_matmul(d["Xd"], c.threshold, Wq, sw, None, Wd, Y=d["Y"], workspace=d["ws"])
+            hY[ci].copy_(d["Y"], non_blocking=True)
+
+    def timed(fn, n):
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ev_a.record()
+        for i in range(n):
+            fn(i)
+        ev_b.record()
+        torch.cuda.synchronize()
+        ms = ev_a.elapsed_time(ev_b)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    e2e_ms = timed(e2e_step, args.steps)
+    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+    G2 = min(args.steps, 8)
+    e2e_graphs = []
+    for gi in range(G2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            e2e_step(gi)
+        e2e_graphs.append(g)
+    e2e_graph_ms = timed(lambda i: e2e_graphs[i % G2].replay(), args.steps)
+    e2e_graph_value = total_bytes / (e2e_graph_ms * 1e-3) / 1e9
+    del e2e_graphs
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # ---- prefill calls (context in the same line): TOPS of the call and of the GEMM stage
+    prefill = None
+    if not args.no_prefill:
+        prefill = run_prefill(args, dev, stream, bf16_peak, peak_src)
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu:
+            b, t, reps, threads = cpu_oracle_time([(d["c"].M, d["c"].K, d["c"].N, d["X"], d["W"]) for d in cases])
+            cpu = {"value": b / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                   "sample": f"the 9 decode calls of one step, repeated {reps}x ({t:.1f} s of oracle time; "
+                             f"A1..A5 per call, weights quantized beforehand)"}
+        trec = traffic_record("gemv.cuh")
+        traffic = None if trec is None else trec["dram_bytes_per_launch"]
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "calls_per_step": ncase, "weight_replicas": R,
+                       "launch": "each step is one CUDA graph of the 9 calls (replayed; captured beforehand)",
+                       "l2": (f"inputs larger than L2: {R} rotating weight replicas; each matrix is re-read only "
+                              f"after >= {(R - 1) * weight_set / 2**20:.0f} MB of other weights (L2 126 MB)"),
+                       "outliers_per_call": [d["n_o"] for d in cases], "bytes_per_step": step_bytes},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "k_gemv_decode",
+                         "alg_bytes_per_launch": step_bytes / ncase,
+                         "launch_us_avg": 1e3 * gemv_total_ms / gemv_launches, "launches_timed": gemv_launches,
+                         "timing": "CUDA events around each GEMV launch in captured steps (GEMV not overlapped "
+                                   "with the X pass); the step value runs the same calls without those events",
+                         "peak_source": f"{peak_src} hbm_gbs (copy, burst)", "per_shape": per_shape},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "mode": "eager: each call issued from Python through the public llmint8_matmul",
+                    "graph_value": e2e_graph_value},
+            "gpu_launches": args.steps * ncase * 3,
+            "clocks": clocks,
+        }
+        if prefill is not None:
+            line["prefill"] = prefill
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return line
+
+
+def run_prefill(args, dev, stream, bf16_peak, peak_src, iters=None):
+    import torch
+    from bit_quantization_matmul_row_b300 import api
+    iters = iters or max(5, min(50, args.steps))
+    out = []
+    tot_flop, tot_call_ms, tot_gemm_ms = 0.0, 0.0, 0.0
+    for c in synthetic.prefill_7b():
+        X, _ = c.x()
+        W, _ = c.w()
+        Xd = torch.from_numpy(X).to(dev)
+        Wd = torch.from_numpy(W).to(dev)
+        Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd)
+        reps = [(Wq, sw, Wq16, Wd), (Wq.clone(), sw.clone(), Wq16.clone(), Wd.clone())]
+        ws = api.make_workspace(c.M, c.K, c.N, dev)
+        Y = torch.empty((c.M, c.N), dtype=torch.float16, device=dev)
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+        e2 = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+
+        def call(i, timed):
+            Wq_, sw_, Wq16_, Wd_ = reps[i % 2]
+            if timed:
+                e0[i].record(stream)
+            api.llmint8_xpass(Xd, c.threshold, c.N, ws, stream=stream)
+            if timed:
+                e1[i].record(stream)
+            api.llmint8_gemm(Xd, c.threshold, Wq_, sw_, Wq16_, Wd_, Y, ws, stream=stream)
+            if timed:
+                e2[i].record(stream)
+
+        for i in range(3):
+            call(i, False)
+        torch.cuda.synchronize()
+        for i in range(iters):
+            call(i, True)
+        torch.cuda.synchronize()
+        call_ms = sum(e0[i].elapsed_time(e2[i]) for i in range(iters)) / iters
+        gemm_ms = sum(e1[i].elapsed_time(e2[i]) for i in range(iters)) / iters
+        flop = 2.0 * c.M * c.N * c.K
+        n_o = api.read_intermediates(ws, c.M, c.K, c.N)["outlier_count"]
+        out.append({"shape": [c.M, c.K, c.N], "outliers": n_o, "call_us": call_ms * 1e3, "gemm_us": gemm_ms * 1e3,
+                    "tops_call": flop / (call_ms * 1e-3) / 1e12, "tops_gemm": flop / (gemm_ms * 1e-3) / 1e12})
+        tot_flop += flop
+        tot_call_ms += call_ms
+        tot_gemm_ms += gemm_ms
+        del reps, Wq, sw, Wq16, Wd, Xd, ws, Y
+    torch.cuda.empty_cache()
+    tops = tot_flop / (tot_call_ms * 1e-3) / 1e12
+    tops_gemm = tot_flop / (tot_gemm_ms * 1e-3) / 1e12
+    return {"workload": "7B-like prefill: M=2048, K=4096, N in {4096, 11008}; 0.1% outlier columns; t=6.0",
+            "value": tops, "unit": "TOPS", "iters": iters,
+            "roofline": {"bound": "tensor", "achieved": tops_gemm, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": tops_gemm / bf16_peak, "kernel": "k_gemm_tc",
+                         "peak_source": f"{peak_src} bf16_tflops (cuBLAS, burst); tcgen05 kind::f16 runs at the "
+                                        "bf16 rate; sm_103a has no int8 tcgen05 kind"},
+            "shapes": out}
+
+
+def run_profile(args):
+    """Eager calls of one named case (warmup + steps), for profiler captures."""
+    import torch
+    from bit_quantization_matmul_row_b300 import api
+    allc = {c.name: c for c in (synthetic.tiny() + synthetic.decode_7b() + synthetic.prefill_7b() +
+                                 synthetic.ffn_13b() + synthetic.sweep_70b())}
+    if args.profile not in allc:
+        raise SystemExit(f"unknown case {args.profile}; known: {sorted(allc)}")
+    c = allc[args.profile]
+    X, _ = c.x()
+    W, _ = c.w()
+    dev = torch.device("cuda")
+    Xd, Wd = torch.from_numpy(X).to(dev), torch.from_numpy(W).to(dev)
+    Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd, fp16_codes=c.M > 16)
+    ws = api.make_workspace(c.M, c.K, c.N, dev)
+    Y = torch.empty((c.M, c.N), dtype=torch.float16, device=dev)
+    for _ in range(args.warmup):
+        api.llmint8_matmul(Xd, c.threshold, Wq, sw, Wq16, Wd, Y=Y, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        api.llmint8_matmul(Xd, c.threshold, Wq, sw, Wq16, Wd, Y=Y, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    st = api.llmint8_device_status(ws)
+    print(json.dumps({"profile": c.name, "calls": args.steps, "us_per_call": 1e3 * e0.elapsed_time(e1) / args.steps,
+                      "status": st}), flush=True)
+    if st != 0:
+        raise SystemExit(1)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--replicas", type=int, default=4)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--max-graphs", type=int, default=256)
+    ap.add_argument("--profile", metavar="CASE", default=None,
+                    help="run only the named synthetic case (eager calls; for ncu captures)")
+    args = ap.parse_args()
+    if args.warmup < 3 and not args.profile:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.profile:
+        run_profile(args)
+        return
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -20,6 +20,8 @@ EXPORTS = (
     "llmint8_matmul",
     "llmint8_matmul_int8",
     "llmint8_matmul_i32",
+    "llmint8_xpass",
+    "llmint8_gemm",
     "llmint8_workspace_layout",
     "llmint8_device_status",
     "llmint8_selftest_timeout",
@@ -49,11 +51,13 @@ def load() -> ctypes.CDLL:
         lib.llmint8_matmul.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_int8.argtypes = [P, I, I, I, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_i32.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
+        lib.llmint8_xpass.argtypes = [P, I, I, I, F, P, Z, P]
+        lib.llmint8_gemm.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
         lib.llmint8_workspace_layout.argtypes = [I, I, I, ctypes.POINTER(Z)]
         lib.llmint8_device_status.argtypes = [P, P]
         lib.llmint8_selftest_timeout.argtypes = [P, I, P]
         for f in ("llmint8_quantize_weight", "llmint8_matmul", "llmint8_matmul_int8", "llmint8_matmul_i32",
-                  "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
+                  "llmint8_xpass", "llmint8_gemm", "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
             getattr(lib, f).restype = I
         _lib = lib
         return lib

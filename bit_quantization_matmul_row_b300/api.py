@@ -135,6 +135,25 @@ def llmint8_matmul_i32(X, threshold, Wq, colScaleW, Wq16, C=None, workspace=None
     return C
 
 
+def llmint8_xpass(X, threshold, N, workspace, stream=None):
+    """A1 + A2 into `workspace` (first half of llmint8_matmul)."""
+    M, K = X.shape
+    _need(X, torch.float16, (M, K), "X")
+    st = _lib.load().llmint8_xpass(_ptr(X), M, K, int(N), float(threshold), _ptr(workspace), workspace.numel(),
+                                   _stream(stream))
+    _check(st, "llmint8_xpass")
+
+
+def llmint8_gemm(X, threshold, Wq, colScaleW, Wq16, W16, Y, workspace, stream=None):
+    """A3..A5 from a workspace filled by llmint8_xpass (second half of llmint8_matmul)."""
+    M, K, N = _shapes(X, Wq)
+    _need(Y, torch.float16, (M, N), "Y")
+    st = _lib.load().llmint8_gemm(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
+                                  _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "llmint8_gemm")
+    return Y
+
+
 def llmint8_device_status(workspace, stream=None) -> int:
     """Synchronize and read (then clear) the device error word; returns a status code."""
     return int(_lib.load().llmint8_device_status(_ptr(workspace), _stream(stream)))
@@ -156,10 +175,14 @@ def read_intermediates(workspace: torch.Tensor, M: int, K: int, N: int) -> dict:
     count = int(ws[lay["outlier_count"]:lay["outlier_count"] + 4].view(torch.int32).item())
     idx = ws[lay["outlier_idx"]:lay["outlier_idx"] + 4 * count].view(torch.int32).clone()
     row_scale = ws[lay["row_scale"]:lay["row_scale"] + 4 * M].view(torch.float32).clone()
-    codes16 = ws[lay["codes"]:lay["codes"] + 2 * M * K].view(torch.float16).view(M, K)
-    codes = codes16.to(torch.int8)
+    if M <= _lib.DECODE_MAX_M:  # decode path: int8 codes
+        codes = ws[lay["codes"]:lay["codes"] + M * K].view(torch.int8).view(M, K).clone()
+        codes16 = None
+    else:  # tensor-core path: the codes as exact fp16 values
+        codes16 = ws[lay["codes"]:lay["codes"] + 2 * M * K].view(torch.float16).view(M, K).clone()
+        codes = codes16.to(torch.int8)
     status = int(ws[lay["status"]:lay["status"] + 4].view(torch.int32).item())
-    return dict(row_scale=row_scale, codes=codes, codes_fp16=codes16.clone(), outliers=idx,
+    return dict(row_scale=row_scale, codes=codes, codes_fp16=codes16, outliers=idx,
                 outlier_count=count, status=status)
 
 

@@ -29,6 +29,7 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     bool gemm_attr_set = false;
+    bool gemv_attr_set = false;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -105,7 +106,7 @@ Layout make_layout(int M, int K, int N) {
     L.codes = off;
     off = align_up(off + (size_t)M * K * 2, 256);
     L.xo = off;
-    if (!L.decode) off = align_up(off + (size_t)M * L.kp * 2, 256);
+    off = align_up(off + (size_t)M * L.kp * 2, 256);
     L.w16o = off;
     if (!L.decode) off = align_up(off + (size_t)N * L.kp * 2, 256);
     L.total = off;
@@ -119,6 +120,25 @@ llmint8_status launch_status() {
     return e == cudaSuccess ? LLMINT8_OK : LLMINT8_ECUDA;
 }
 
+// Launch with the programmatic stream-serialization attribute when `pdl`: the
+// kernel may start while its predecessor in the stream is still running and
+// synchronizes with it through griddepcontrol.wait (pdl_wait in the kernels).
+template <typename... KArgs, typename... Args>
+llmint8_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? LLMINT8_OK : LLMINT8_ECUDA;
+}
+
 int row_quant_vpt(int K) {
     const int nvec = K / 8;
     if (nvec <= kRowThreads) return 1;
@@ -128,83 +148,123 @@ int row_quant_vpt(int K) {
     return 0;
 }
 
-llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
-                           const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
-                           void* workspace, size_t ws_bytes, void* stream_) {
-    if (!X || !Wq || !colScaleW || !out) return LLMINT8_EINVAL;
+// Checks shared by every entry point that runs part of the matmul.
+llmint8_status check_common(const void* X, int M, int K, int N, float threshold, void* workspace, size_t ws_bytes,
+                            Layout* L, DeviceInfo** dev) {
+    if (!X) return LLMINT8_EINVAL;
     if (!sizes_ok(M, K, N) || std::isnan(threshold)) return LLMINT8_EINVAL;
+    if ((K % 16) || (N % 16)) return LLMINT8_EALIGN;
+    if (!aligned16(X) || !aligned16(workspace)) return LLMINT8_EALIGN;
+    *L = make_layout(M, K, N);
+    if (!workspace || ws_bytes < L->total) return LLMINT8_EWORKSPACE;
+    return LLMINT8_OK;
+}
+
+// Checks of the GEMM operands.
+llmint8_status check_operands(int M, float threshold, const int8_t* Wq, const float* colScaleW, const void* Wq16,
+                              const void* W16, const void* out, bool write_i32) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
     const bool decode = M <= LLMINT8_DECODE_MAX_M;
+    if (!Wq || !colScaleW || !out) return LLMINT8_EINVAL;
     if (use_outliers && !W16 && !write_i32) return LLMINT8_EINVAL;
     if (!decode && !Wq16) return LLMINT8_EINVAL;
-    if ((K % 16) || (N % 16)) return LLMINT8_EALIGN;
-    if (!aligned16(X) || !aligned16(Wq) || !aligned16(colScaleW) || !aligned16(out) ||
-        (Wq16 && !aligned16(Wq16)) || (W16 && !aligned16(W16)) || !aligned16(workspace))
+    if (!aligned16(Wq) || !aligned16(colScaleW) || !aligned16(out) || (Wq16 && !aligned16(Wq16)) ||
+        (W16 && !aligned16(W16)))
         return LLMINT8_EALIGN;
-    const Layout L = make_layout(M, K, N);
-    if (!workspace || ws_bytes < L.total) return LLMINT8_EWORKSPACE;
-    DeviceInfo* dev = nullptr;
-    llmint8_status st = current_device(&dev);
-    if (st != LLMINT8_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream_);
+    return LLMINT8_OK;
+}
 
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.hdr);
-    uint32_t* bitmap = reinterpret_cast<uint32_t*>(ws + L.bitmap);
-    int32_t* idx = reinterpret_cast<int32_t*>(ws + L.idx);
-    float* row_scale = reinterpret_cast<float*>(ws + L.row_scale);
-    __half* codes = reinterpret_cast<__half*>(ws + L.codes);
-    __half* xo = reinterpret_cast<__half*>(ws + L.xo);
-    __half* w16o = reinterpret_cast<__half*>(ws + L.w16o);
+struct WsView {
+    WsHeader* hdr;
+    uint32_t* bitmap;
+    int32_t* idx;
+    float* row_scale;
+    __half* codes;
+    __half* xo;
+    __half* w16o;
+    WsView(void* workspace, const Layout& L) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        hdr = reinterpret_cast<WsHeader*>(ws + L.hdr);
+        bitmap = reinterpret_cast<uint32_t*>(ws + L.bitmap);
+        idx = reinterpret_cast<int32_t*>(ws + L.idx);
+        row_scale = reinterpret_cast<float*>(ws + L.row_scale);
+        codes = reinterpret_cast<__half*>(ws + L.codes);
+        xo = reinterpret_cast<__half*>(ws + L.xo);
+        w16o = reinterpret_cast<__half*>(ws + L.w16o);
+    }
+};
+
+// A1 + A2 into the workspace.
+llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* workspace, const Layout& L,
+                            const DeviceInfo* dev, cudaStream_t s) {
+    const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
+    const WsView w(workspace, L);
     const __half* Xh = static_cast<const __half*>(X);
+    llmint8_status st;
 
-    // the header (error word, outlier count) and the outlier bit map start at zero:
-    // the error word reports this call
-    if (cudaMemsetAsync(ws + L.hdr, 0, L.idx - L.hdr, s) != cudaSuccess) return LLMINT8_ECUDA;
-
-    // A1: outlier columns
-    if (use_outliers) {
-        const int gx = (K + kScanCols - 1) / kScanCols;
-        int gy = (M + 7) / 8;
+    // A1: outlier columns.  With one row group (always for M <= 64) each scan CTA
+    // stores its bitmap words directly and CTA 0 resets the error word; with
+    // several row groups the words are OR-ed atomically into a zeroed map.
+    const int gx = (K + kScanCols - 1) / kScanCols;
+    int gy = 1;
+    if (M > 64) {
+        gy = (M + 7) / 8;
         const int cap = (dev->sms * 8 + gx - 1) / gx;
         if (gy > cap) gy = cap;
         if (gy < 1) gy = 1;
-        k_outlier_scan<<<dim3(gx, gy), kScanThreads, 0, s>>>(Xh, M, K, threshold, bitmap);
-        if ((st = launch_status()) != LLMINT8_OK) return st;
+    }
+    if (use_outliers) {
+        if (gy > 1 && cudaMemsetAsync(static_cast<uint8_t*>(workspace) + L.hdr, 0, L.idx - L.hdr, s) != cudaSuccess)
+            return LLMINT8_ECUDA;
+        st = launch(k_outlier_scan, dim3(gx, gy), dim3(kScanThreads), 0, s, true, Xh, M, K, threshold, w.bitmap,
+                    gy > 1 ? nullptr : w.hdr);
+        if (st != LLMINT8_OK) return st;
     }
 
-    // A2: row scales and codes (+ gathered outlier columns for the tensor-core path)
+    // A2: row scales and codes (+ the gathered outlier columns of X)
     RowQuantArgs ra;
     ra.X = Xh;
     ra.M = M;
     ra.K = K;
-    ra.bitmap = bitmap;
-    ra.hdr = hdr;
-    ra.outlier_idx = idx;
-    ra.row_scale = row_scale;
-    ra.codes = codes;
-    ra.xo = (!decode && use_outliers) ? xo : nullptr;
+    ra.bitmap = w.bitmap;
+    ra.hdr = w.hdr;
+    ra.outlier_idx = w.idx;
+    ra.row_scale = w.row_scale;
+    ra.codes = w.codes;
+    ra.codes_fp16 = L.decode ? 0 : 1;  // int8 for the decode GEMV, fp16 values for the tensor-core GEMM
+    ra.xo = use_outliers ? w.xo : nullptr;
     ra.xo_pitch = L.kp;
+    ra.no_outliers = use_outliers ? 0 : 1;
+    ra.clear_status = use_outliers ? 0 : 1;
+    const bool pdl = true;
     switch (row_quant_vpt(K)) {
-        case 1: k_row_quant<1><<<M, kRowThreads, 0, s>>>(ra); break;
-        case 2: k_row_quant<2><<<M, kRowThreads, 0, s>>>(ra); break;
-        case 4: k_row_quant<4><<<M, kRowThreads, 0, s>>>(ra); break;
-        case 8: k_row_quant<8><<<M, kRowThreads, 0, s>>>(ra); break;
-        default: k_row_quant<0><<<M, kRowThreads, 0, s>>>(ra); break;
+        case 1: return launch(k_row_quant<1>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
+        case 2: return launch(k_row_quant<2>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
+        case 4: return launch(k_row_quant<4>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
+        case 8: return launch(k_row_quant<8>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
+        default: return launch(k_row_quant<0>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
     }
-    if ((st = launch_status()) != LLMINT8_OK) return st;
+}
 
-    if (decode) {
-        // A3-A5, decode GEMV
+// A3 + A4 + A5 from the workspace an xpass_launch of the same problem filled.
+llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
+                           const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
+                           void* workspace, const Layout& L, DeviceInfo* dev, cudaStream_t s) {
+    const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
+    const WsView w(workspace, L);
+    llmint8_status st;
+
+    if (L.decode) {
         GemvArgs ga;
-        ga.codes = codes;
+        ga.codes = reinterpret_cast<const int8_t*>(w.codes);
         ga.Wq = Wq;
         ga.col_scale = colScaleW;
-        ga.row_scale = row_scale;
-        ga.X = Xh;
+        ga.row_scale = w.row_scale;
         ga.W16 = static_cast<const __half*>(W16);
-        ga.hdr = hdr;
-        ga.outlier_idx = idx;
+        ga.hdr = w.hdr;
+        ga.outlier_idx = w.idx;
+        ga.xo = w.xo;
+        ga.xo_pitch = L.kp;
         ga.out = out;
         ga.M = M;
         ga.K = K;
@@ -212,29 +272,43 @@ llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, 
         const int ksteps = (K + 63) / 64;
         ga.k_per_warp = ((ksteps + kGemvWarps - 1) / kGemvWarps) * 64;
         ga.use_outliers = use_outliers ? 1 : 0;
-        const dim3 grid(N / kGemvCols);
-        if (M <= 8) {
-            if (write_i32) k_gemv_decode<1, true><<<grid, kGemvWarps * 32, 0, s>>>(ga);
-            else k_gemv_decode<1, false><<<grid, kGemvWarps * 32, 0, s>>>(ga);
-        } else {
-            if (write_i32) k_gemv_decode<2, true><<<grid, kGemvWarps * 32, 0, s>>>(ga);
-            else k_gemv_decode<2, false><<<grid, kGemvWarps * 32, 0, s>>>(ga);
+        {
+            std::lock_guard<std::mutex> lock(g_mu);
+            if (!dev->gemv_attr_set) {
+                const int sm = (int)kGemvDynSmem;
+                if (cudaFuncSetAttribute(k_gemv_decode<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=
+                        cudaSuccess)
+                    return LLMINT8_ECUDA;
+                dev->gemv_attr_set = true;
+            }
         }
-        return launch_status();
+        const dim3 grid(N / kGemvCols), block(kGemvWarps * 32);
+        const size_t dyn = kGemvDynSmem;
+        if (M <= 8)
+            return write_i32 ? launch(k_gemv_decode<1, true>, grid, block, dyn, s, true, ga)
+                             : launch(k_gemv_decode<1, false>, grid, block, dyn, s, true, ga);
+        return write_i32 ? launch(k_gemv_decode<2, true>, grid, block, dyn, s, true, ga)
+                         : launch(k_gemv_decode<2, false>, grid, block, dyn, s, true, ga);
     }
 
     // A4 operand: gathered, transposed outlier rows of W16
     if (use_outliers && !write_i32) {
-        k_gather_w16_outlier_rows<<<(N + 63) / 64, 256, 0, s>>>(static_cast<const __half*>(W16), N, hdr, idx, w16o,
-                                                                L.kp);
-        if ((st = launch_status()) != LLMINT8_OK) return st;
+        st = launch(k_gather_w16_outlier_rows, dim3((N + 63) / 64), dim3(256), 0, s, true,
+                    static_cast<const __half*>(W16), N, (const WsHeader*)w.hdr, (const int32_t*)w.idx, w.w16o, L.kp);
+        if (st != LLMINT8_OK) return st;
     }
     if ((st = get_encoder()) != LLMINT8_OK) return st;
     CUtensorMap tm_a, tm_b, tm_xo, tm_wo;
-    if ((st = encode_fp16_2d(&tm_a, codes, M, K, K, kBM)) != LLMINT8_OK) return st;
+    if ((st = encode_fp16_2d(&tm_a, w.codes, M, K, K, kBM)) != LLMINT8_OK) return st;
     if ((st = encode_fp16_2d(&tm_b, Wq16, N, K, K, kBN)) != LLMINT8_OK) return st;
-    if ((st = encode_fp16_2d(&tm_xo, xo, M, L.kp, L.kp, kBM)) != LLMINT8_OK) return st;
-    if ((st = encode_fp16_2d(&tm_wo, w16o, N, L.kp, L.kp, kBN)) != LLMINT8_OK) return st;
+    if ((st = encode_fp16_2d(&tm_xo, w.xo, M, L.kp, L.kp, kBM)) != LLMINT8_OK) return st;
+    if ((st = encode_fp16_2d(&tm_wo, w.w16o, N, L.kp, L.kp, kBN)) != LLMINT8_OK) return st;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!dev->gemm_attr_set) {
@@ -247,10 +321,10 @@ llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, 
         }
     }
     GemmArgs ga;
-    ga.row_scale = row_scale;
+    ga.row_scale = w.row_scale;
     ga.col_scale = colScaleW;
-    ga.hdr = hdr;
-    ga.err = hdr;
+    ga.hdr = w.hdr;
+    ga.err = w.hdr;
     ga.out = out;
     ga.M = M;
     ga.N = N;
@@ -261,10 +335,23 @@ llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, 
     const int ntiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     const int grid = ntiles < dev->sms ? ntiles : dev->sms;
     if (write_i32)
-        k_gemm_tc<true><<<grid, kGemmThreads, kGemmSmem, s>>>(tm_a, tm_b, tm_xo, tm_wo, ga);
-    else
-        k_gemm_tc<false><<<grid, kGemmThreads, kGemmSmem, s>>>(tm_a, tm_b, tm_xo, tm_wo, ga);
-    return launch_status();
+        return launch(k_gemm_tc<true>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo, tm_wo,
+                      ga);
+    return launch(k_gemm_tc<false>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo, tm_wo, ga);
+}
+
+llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
+                           const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
+                           void* workspace, size_t ws_bytes, void* stream) {
+    Layout L;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = check_common(X, M, K, N, threshold, workspace, ws_bytes, &L, &dev);
+    if (st != LLMINT8_OK) return st;
+    if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, out, write_i32)) != LLMINT8_OK) return st;
+    if ((st = current_device(&dev)) != LLMINT8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = xpass_launch(X, M, K, threshold, workspace, L, dev, s)) != LLMINT8_OK) return st;
+    return gemm_launch(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, out, write_i32, workspace, L, dev, s);
 }
 
 // Waits on a barrier nothing completes, bounded by spin_limit polls, then
@@ -347,6 +434,29 @@ llmint8_status llmint8_matmul_i32(const void* X, int M, int K, int N, float thre
                                   size_t workspace_bytes, void* stream) {
     return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, nullptr, C, true, workspace, workspace_bytes,
                        stream);
+}
+
+llmint8_status llmint8_xpass(const void* X, int M, int K, int N, float threshold, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    Layout L;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = check_common(X, M, K, N, threshold, workspace, workspace_bytes, &L, &dev);
+    if (st != LLMINT8_OK) return st;
+    if ((st = current_device(&dev)) != LLMINT8_OK) return st;
+    return xpass_launch(X, M, K, threshold, workspace, L, dev, static_cast<cudaStream_t>(stream));
+}
+
+llmint8_status llmint8_gemm(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
+                            const float* colScaleW, const void* Wq16, const void* W16, void* Y, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    Layout L;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = check_common(X, M, K, N, threshold, workspace, workspace_bytes, &L, &dev);
+    if (st != LLMINT8_OK) return st;
+    if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, Y, false)) != LLMINT8_OK) return st;
+    if ((st = current_device(&dev)) != LLMINT8_OK) return st;
+    return gemm_launch(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, L, dev,
+                       static_cast<cudaStream_t>(stream));
 }
 
 llmint8_status llmint8_workspace_layout(int M, int K, int N, size_t* offsets) {

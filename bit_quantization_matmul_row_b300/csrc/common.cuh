@@ -59,6 +59,18 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     return v;
 }
 
+// L2-coherent load (bypasses L1).  Used for every buffer an earlier kernel of
+// the same call writes: with programmatic dependent launch the reading kernel is
+// already running while that buffer is produced, so the non-coherent read-only
+// path (ld.global.nc), whose data must not change during the reader's lifetime,
+// is not allowed for it.
+__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+    return v;
+}
+
 // Streaming load that does not allocate in L1 (weights are read exactly once).
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
     uint4 v;
@@ -67,11 +79,24 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
     return v;
 }
 
+// Asynchronous 16-byte global -> shared copies (completion per thread via wait_all).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src);
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

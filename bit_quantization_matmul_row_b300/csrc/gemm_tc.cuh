@@ -23,6 +23,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "xpass.cuh"
 
 namespace llmint8 {
 
@@ -73,9 +74,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int ntiles = tiles_m * tiles_n;
     const int ksteps = (a.K + kBK - 1) / kBK;
     const int nchunks_int = (ksteps + kChunkSteps - 1) / kChunkSteps;
-    const int n_out = a.use_outliers ? a.hdr->outlier_count : 0;
-    const int osteps = (n_out + kBK - 1) / kBK;
 
+    // set-up that does not depend on the X pass overlaps its tail (programmatic
+    // dependent launch); everything after pdl_wait() may read its results
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ss->full[s], 1);
@@ -90,7 +92,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
-        if (osteps) {
+        if (a.use_outliers) {
             tma_prefetch_desc(&tm_xo);
             tma_prefetch_desc(&tm_wo);
         }
@@ -103,6 +105,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ss->tmem_base;
+    pdl_wait();
+    const int n_out = a.use_outliers ? __ldcg(&a.hdr->outlier_count) : 0;
+    const int osteps = (n_out + kBK - 1) / kBK;
 
     auto fail = [&](uint32_t where) {
         *abort_flag = 1u;
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_fence_after();
             }
             const bool row_ok = row < a.M;
-            const float sx = row_ok ? a.row_scale[row] * (1.0f / 16129.0f) : 0.0f;
+            const float sx = row_ok ? __ldcg(a.row_scale + row) * (1.0f / 16129.0f) : 0.0f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 uint32_t r[16];

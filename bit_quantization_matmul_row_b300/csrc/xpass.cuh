@@ -11,8 +11,9 @@
 // set, so the pass is two kernels: a scan that ORs per-column flags into a bit
 // map (atomics only for words that hold an outlier, which is rare), then one
 // CTA per row that re-reads its row (from L2 when X fits there) and writes the
-// codes.  Codes are written as fp16 values (exact integers in [-127, 127]) --
-// the operand format of both GEMM paths on sm_103a, which has no int8 tcgen05.
+// codes: as int8 for the decode GEMV (int8 mma.sync), or as fp16 values (exact
+// integers in [-127, 127]) for the tensor-core GEMM (sm_103a has no int8
+// tcgen05 kind).
 #pragma once
 
 #include "common.cuh"
@@ -35,9 +36,30 @@ __device__ __forceinline__ uint32_t outlier_mask8(uint4 v, float t) {
     return m;
 }
 
-// A1.  grid = (ceil(K/256), row groups); bitmap must be zero on entry.
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before its predecessor finishes;
+// pdl_wait() blocks until the predecessor has completed and its writes are
+// visible (a no-op for a normal launch), pdl_trigger() lets the successor start.
+// Every kernel of a call is launched this way, the first one included, so a
+// call's kernels (and the weight prefetch of its GEMV) may start while the
+// previous call's last kernel drains.  Rule that keeps this safe: before
+// pdl_wait() a kernel reads nothing but the weights (constant inputs) and
+// writes nothing outside its own shared memory; X and the workspace are
+// touched only after it, and through L2 (ld.global.cg), since the
+// non-coherent read-only path requires data that no running kernel writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// A1.  grid = (ceil(K/256), row groups).  With one row group (gridDim.y == 1)
+// every CTA sees all rows of its columns and stores its bitmap words directly;
+// with several, the words are OR-ed atomically and the bitmap must be zero on
+// entry.  `hdr`, when given, has its error word cleared by CTA 0 (the first
+// kernel of a call resets the word).
 __global__ void __launch_bounds__(kScanThreads) k_outlier_scan(const __half* __restrict__ X, int M, int K, float t,
-                                                               uint32_t* __restrict__ bitmap) {
+                                                               uint32_t* __restrict__ bitmap, WsHeader* hdr) {
+    pdl_trigger();
+    pdl_wait();
+    if (hdr != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->status = 0u;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c0 = blockIdx.x * kScanCols + lane * 8;
     uint32_t m = 0;
@@ -47,11 +69,11 @@ __global__ void __launch_bounds__(kScanThreads) k_outlier_scan(const __half* __r
         const int step = gridDim.y * 8;
         // two independent loads in flight per iteration
         for (; r + step < M; r += 2 * step) {
-            const uint4 a = ldg_nc_v4(p + (size_t)r * K);
-            const uint4 b = ldg_nc_v4(p + (size_t)(r + step) * K);
+            const uint4 a = ldg_cg_v4(p + (size_t)r * K);
+            const uint4 b = ldg_cg_v4(p + (size_t)(r + step) * K);
             m |= outlier_mask8(a, t) | outlier_mask8(b, t);
         }
-        if (r < M) m |= outlier_mask8(ldg_nc_v4(p + (size_t)r * K), t);
+        if (r < M) m |= outlier_mask8(ldg_cg_v4(p + (size_t)r * K), t);
     }
     // lanes 4w..4w+3 hold the 32 columns of bitmap word w of this strip
     uint32_t word = m << (8 * (lane & 3));
@@ -65,7 +87,12 @@ __global__ void __launch_bounds__(kScanThreads) k_outlier_scan(const __half* __r
 #pragma unroll
         for (int w = 0; w < 8; ++w) acc |= s_words[w][threadIdx.x];
         const int gw = blockIdx.x * (kScanCols / 32) + threadIdx.x;
-        if (acc != 0u && gw < (K + 31) / 32) atomicOr(&bitmap[gw], acc);
+        if (gw < (K + 31) / 32) {
+            if (gridDim.y == 1)
+                bitmap[gw] = acc;
+            else if (acc != 0u)
+                atomicOr(&bitmap[gw], acc);
+        }
     }
 }
 
@@ -80,9 +107,12 @@ struct RowQuantArgs {
     WsHeader* hdr;            // outlier_count written by block 0
     int32_t* outlier_idx;     // [K], written by block 0
     float* row_scale;         // [M]
-    __half* codes;            // [M, K]
+    void* codes;              // [M, K]: int8, or fp16 values when codes_fp16
+    int codes_fp16;
     __half* xo;               // [M, xo_pitch] gathered outlier columns (nullptr: skip)
     int xo_pitch;             // elements; gathered columns are zero-padded up to a multiple of 64
+    int no_outliers;          // threshold +inf: no scan ran, the bit map is not read
+    int clear_status;         // no earlier kernel of this call reset the error word
 };
 
 // Round half away from zero, then clamp to [-127, 127] (clamp after rounding,
@@ -107,6 +137,20 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
     const int row = blockIdx.x;
     const int K = a.K;
     const int nwords = (K + 31) >> 5;
+    pdl_trigger();
+    pdl_wait();
+
+    const __half* xrow = a.X + (size_t)row * K;
+    const int nvec = K >> 3;  // K % 16 == 0
+    uint4 v[VPT > 0 ? VPT : 1];
+    if (VPT > 0) {
+#pragma unroll
+        for (int i = 0; i < (VPT > 0 ? VPT : 1); ++i) {
+            const int vi = tid + i * kRowThreads;
+            if (vi < nvec) v[i] = ldg_cg_v4(xrow + (size_t)vi * 8);
+        }
+    }
+    if (a.clear_status && row == 0 && tid == 0) a.hdr->status = 0u;
 
     // --- bitmap -> shared memory, exclusive prefix of popcounts (block scan) ---
     constexpr int WPT = kMaxWords / kRowThreads;  // words per thread (8)
@@ -115,7 +159,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
 #pragma unroll
     for (int i = 0; i < WPT; ++i) {
         const int w = tid * WPT + i;
-        const uint32_t b = (w < nwords) ? a.bitmap[w] : 0u;
+        const uint32_t b = (w < nwords && !a.no_outliers) ? __ldcg(a.bitmap + w) : 0u;
         if (w < nwords) s_bits[w] = b;
         local[i] = __popc(b);
         tsum += local[i];
@@ -149,9 +193,6 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
     const int n_out = s_total;
 
     // --- masked absmax over the non-outlier columns of this row ---
-    const __half* xrow = a.X + (size_t)row * K;
-    const int nvec = K >> 3;  // K % 16 == 0
-    uint4 v[VPT > 0 ? VPT : 1];
     float amax = 0.0f;
     auto absmax_vec = [&](uint4 x, int c) {
         const uint32_t om = (s_bits[c >> 5] >> (c & 31)) & 0xFFu;
@@ -167,15 +208,10 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
 #pragma unroll
         for (int i = 0; i < (VPT > 0 ? VPT : 1); ++i) {
             const int vi = tid + i * kRowThreads;
-            if (vi < nvec) v[i] = ldg_nc_v4(xrow + (size_t)vi * 8);
-        }
-#pragma unroll
-        for (int i = 0; i < (VPT > 0 ? VPT : 1); ++i) {
-            const int vi = tid + i * kRowThreads;
             if (vi < nvec) absmax_vec(v[i], vi * 8);
         }
     } else {
-        for (int vi = tid; vi < nvec; vi += kRowThreads) absmax_vec(ldg_nc_v4(xrow + (size_t)vi * 8), vi * 8);
+        for (int vi = tid; vi < nvec; vi += kRowThreads) absmax_vec(ldg_cg_v4(xrow + (size_t)vi * 8), vi * 8);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -189,20 +225,35 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
     const float sf = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
 
     // --- codes (outlier columns -> 0) ---
-    __half* crow = a.codes + (size_t)row * K;
     auto code_vec = [&](uint4 x, int c) {
         const uint32_t om = (s_bits[c >> 5] >> (c & 31)) & 0xFFu;
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint32_t o[4];
+        float q[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-            const float q0 = ((om >> (2 * e)) & 1u) ? 0.0f : code_of(f.x, sf);
-            const float q1 = ((om >> (2 * e + 1)) & 1u) ? 0.0f : code_of(f.y, sf);
-            __half2 h = __floats2half2_rn(q0, q1);
-            o[e] = *reinterpret_cast<uint32_t*>(&h);
+            q[2 * e] = ((om >> (2 * e)) & 1u) ? 0.0f : code_of(f.x, sf);
+            q[2 * e + 1] = ((om >> (2 * e + 1)) & 1u) ? 0.0f : code_of(f.y, sf);
         }
-        *reinterpret_cast<uint4*>(crow + c) = make_uint4(o[0], o[1], o[2], o[3]);
+        if (a.codes_fp16) {
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __half2 h = __floats2half2_rn(q[2 * e], q[2 * e + 1]);
+                o[e] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            __half* crow = static_cast<__half*>(a.codes) + (size_t)row * K;
+            *reinterpret_cast<uint4*>(crow + c) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            uint32_t o[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                o[e] = ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e]) | ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 1] << 8) |
+                       ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 2] << 16) |
+                       ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 3] << 24);
+            int8_t* crow = static_cast<int8_t*>(a.codes) + (size_t)row * K;
+            *reinterpret_cast<uint2*>(crow + c) = make_uint2(o[0], o[1]);
+        }
     };
     if (VPT > 0) {
 #pragma unroll
@@ -211,7 +262,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
             if (vi < nvec) code_vec(v[i], vi * 8);
         }
     } else {
-        for (int vi = tid; vi < nvec; vi += kRowThreads) code_vec(ldg_nc_v4(xrow + (size_t)vi * 8), vi * 8);
+        for (int vi = tid; vi < nvec; vi += kRowThreads) code_vec(ldg_cg_v4(xrow + (size_t)vi * 8), vi * 8);
     }
     if (tid == 0) a.row_scale[row] = amax;
 
@@ -225,7 +276,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
                 const int bit = __ffs(b) - 1;
                 b &= b - 1;
                 const int col = w * 32 + bit;
-                if (xo_row) xo_row[pos] = xrow[col];
+                if (xo_row) xo_row[pos] = __ldcg(xrow + col);
                 if (row == 0) a.outlier_idx[pos] = col;
                 ++pos;
             }
@@ -249,7 +300,9 @@ __global__ void __launch_bounds__(256) k_gather_w16_outlier_rows(const __half* _
                                                                  const int32_t* __restrict__ outlier_idx,
                                                                  __half* __restrict__ w16oT, int pitch) {
     __shared__ __half tile[64][64 + 8];
-    const int count = hdr->outlier_count;
+    pdl_trigger();
+    pdl_wait();
+    const int count = __ldcg(&hdr->outlier_count);
     const int padded = (count + 63) & ~63;
     const int n0 = blockIdx.x * 64;
     const int tid = threadIdx.x;
@@ -259,7 +312,7 @@ __global__ void __launch_bounds__(256) k_gather_w16_outlier_rows(const __half* _
             const int pr = e >> 6, nc = e & 63;
             const int p = p0 + pr, n = n0 + nc;
             __half v = __ushort_as_half(0);
-            if (p < count && n < N) v = W16[(size_t)outlier_idx[p] * N + n];
+            if (p < count && n < N) v = W16[(size_t)__ldcg(outlier_idx + p) * N + n];
             tile[pr][nc] = v;
         }
         __syncthreads();

@@ -115,6 +115,28 @@ llmint8_status llmint8_matmul_int8(const void *X, int M, int K, int N, const int
                                    const float *colScaleW, const void *Wq16, void *Y,
                                    void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * The two halves of llmint8_matmul, for callers that schedule them apart (and
+ * for timing the GEMM stage alone).  llmint8_matmul(args) enqueues exactly
+ * llmint8_xpass(X, M, K, N, threshold, workspace) followed by
+ * llmint8_gemm(args) on the same stream.
+ *
+ * llmint8_xpass -- steps A1 and A2 (paper walkthrough, sections 2.1 and 2.3):
+ *   reads X fp16 [M, K]; writes into `workspace` the outlier column set, the row
+ *   scales, the codes (see llmint8_workspace_layout) and, for M > 16, the
+ *   gathered outlier columns of X.  Same argument rules as llmint8_matmul.
+ *
+ * llmint8_gemm -- steps A3, A4 and A5 (pitfalls guide, sections 3.2-3.3):
+ *   consumes a workspace that an llmint8_xpass with the same X, M, K, N and
+ *   threshold filled earlier on the same stream (undefined otherwise); X is read
+ *   again for the outlier values.  Writes Y fp16 [M, N].
+ */
+llmint8_status llmint8_xpass(const void *X, int M, int K, int N, float threshold, void *workspace,
+                             size_t workspace_bytes, void *stream);
+llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold, const int8_t *Wq,
+                            const float *colScaleW, const void *Wq16, const void *W16, void *Y,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
 /* ----------------------------------------------------------------------------
  * Introspection (tests and diagnostics; not on the hot path)
  * ------------------------------------------------------------------------- */
@@ -138,8 +160,9 @@ enum {
     LLMINT8_WS_OUTLIER_COUNT = 1,/* int32: number of outlier columns found by the last call */
     LLMINT8_WS_OUTLIER_IDX = 2,  /* int32 [count]: outlier column indices, ascending */
     LLMINT8_WS_ROW_SCALE = 3,    /* fp32 [M]: rowScaleX (absmax over non-outlier columns) */
-    LLMINT8_WS_CODES = 4,        /* fp16 [M, K] row-major: the int8 codes of X stored as
-                                    exact fp16 values (the tensor-core operand format) */
+    LLMINT8_WS_CODES = 4,        /* [M, K] row-major codes of X: int8 when M <= 16 (the
+                                    decode path), else the same codes stored as exact fp16
+                                    values (the tensor-core operand format) */
     LLMINT8_WS_NFIELDS = 5
 };
 

@@ -196,15 +196,20 @@ def outlier_indices(is_outlier: np.ndarray) -> np.ndarray:
 
 
 def llmint8_matmul(X: np.ndarray, W: np.ndarray, t: float, rows=None, nthreads: int | None = None,
-                   wq=None):
+                   wq=None, cols=None):
     """The whole path A0..A5 for Y = X.W with threshold t.
 
     Outlier detection (A1) always scans all rows of X, because the outlier set
     is a property of the whole activation matrix.  ``rows`` (optional index
     array) restricts A2..A5 to those rows, for spot checks of large problems.
-    ``wq`` may pass a precomputed (Wq, s_w) from quantize_weight.
-    Returns a dict with every intermediate.
+    ``cols`` (optional) restricts the output columns: A0 (one scale per output
+    column), A3, A4 and A5 are each local to a column, so the oracle simply
+    runs on W[:, cols].  ``wq`` may pass a precomputed (Wq, s_w) from
+    quantize_weight of the (restricted) W.  Returns a dict with every
+    intermediate.
     """
+    if cols is not None:
+        W = np.ascontiguousarray(W[:, np.asarray(cols)])
     Wq, s_w = wq if wq is not None else quantize_weight(W)
     is_out = outlier_columns(X, t)
     Xs = X if rows is None else np.ascontiguousarray(X[np.asarray(rows)])

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from bit_quantization_matmul_row_b300 import api, synthetic
-from parity import check, run_gpu, sample_rows
+from parity import check, run_gpu, sample_cols, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -116,6 +116,31 @@ def test_workspace_contents_do_not_matter(M):
     assert np.array_equal(a["Y"].view(np.uint16), b["Y"].view(np.uint16))
 
 
+@pytest.mark.parametrize("M,K,N", [(1, 4096, 11008), (16, 4096, 4096), (300, 1088, 400)])
+def test_workspace_reused_by_consecutive_calls(M, K, N):
+    # Back-to-back calls on one stream and one workspace with different X: the
+    # kernels of a call overlap (programmatic dependent launch), so a read of the
+    # previous call's codes, scales or outlier list would give a wrong Y here.
+    import oracle
+    from parity import y_close
+    W, _ = synthetic.make_w(K, N, seed=K + N)
+    dev = torch.device("cuda")
+    Wd = torch.from_numpy(W).to(dev)
+    Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd)
+    ws = api.make_workspace(M, K, N, dev)
+    Xs = [synthetic.make_x(M, K, frac=0.005 * (j + 1), min_count=2 + 3 * j, seed=500 + j)[0] for j in range(3)]
+    Ys = []
+    for X in Xs:
+        Ys.append(api.llmint8_matmul(torch.from_numpy(X).to(dev), 6.0, Wq, sw, Wq16, Wd, workspace=ws))
+    torch.cuda.synchronize()
+    assert api.llmint8_device_status(ws) == 0
+    wq = oracle.quantize_weight(W)
+    for X, Y in zip(Xs, Ys):
+        ref = oracle.llmint8_matmul(X, W, 6.0, wq=wq)
+        ok, ratio = y_close(Y.cpu().numpy(), ref["Y"])
+        assert ok, ratio
+
+
 @pytest.mark.parametrize("M", [16, 300])
 def test_deterministic_and_stream(M):
     X, W = xw(M, 1088, 400, seed=80 + M)
@@ -139,15 +164,16 @@ def test_bounded_wait_reports_timeout():
 
 
 # ------------------------------------------------------------------ full-size workloads
-# Quantization outputs compared in full; C and Y on sampled rows (the oracle
-# computes those rows one by one).  Same entry points and launch configuration
+# X-pass outputs compared in full; weight codes on sampled columns; C and Y on
+# sampled rows x columns (the oracle computes those one by one).  Same entry points and launch configuration
 # as the benchmark.
 
-def _full_case(case, nrows=24):
+def _full_case(case, nrows=24, ncols=96):
     X, planted = case.x()
     W, _ = case.w()
     rows = sample_rows(case.M, nrows, seed=case.seed)
-    g, ref = check(X, W, case.threshold, rows=rows)
+    cols = sample_cols(case.N, ncols, seed=case.seed)
+    g, ref = check(X, W, case.threshold, rows=rows, cols=cols)
     assert set(planted.tolist()) <= set(g["outliers"].tolist())
 
 
