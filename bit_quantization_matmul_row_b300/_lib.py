@@ -22,6 +22,7 @@ EXPORTS = (
     "llmint8_matmul_i32",
     "llmint8_xpass",
     "llmint8_gemm",
+    "llmint8_matmul_noalloc",
     "llmint8_workspace_layout",
     "llmint8_device_status",
     "llmint8_selftest_timeout",
@@ -53,11 +54,12 @@ def load() -> ctypes.CDLL:
         lib.llmint8_matmul_i32.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
         lib.llmint8_xpass.argtypes = [P, I, I, I, F, P, Z, P]
         lib.llmint8_gemm.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
+        lib.llmint8_matmul_noalloc.argtypes = [P, I, I, I, F, P, P, P, P, P, P]
         lib.llmint8_workspace_layout.argtypes = [I, I, I, ctypes.POINTER(Z)]
         lib.llmint8_device_status.argtypes = [P, P]
         lib.llmint8_selftest_timeout.argtypes = [P, I, P]
         for f in ("llmint8_quantize_weight", "llmint8_matmul", "llmint8_matmul_int8", "llmint8_matmul_i32",
-                  "llmint8_xpass", "llmint8_gemm", "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
+                  "llmint8_xpass", "llmint8_gemm", "llmint8_matmul_noalloc", "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
             getattr(lib, f).restype = I
         _lib = lib
         return lib

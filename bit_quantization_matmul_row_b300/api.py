@@ -154,6 +154,23 @@ def llmint8_gemm(X, threshold, Wq, colScaleW, Wq16, W16, Y, workspace, stream=No
     return Y
 
 
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def llmint8_matmul_noalloc(X, threshold, Wq, colScaleW, Wq16, W16, Y, stream=None):
+    """llmint8_matmul on the library's static scratch array (no workspace, no allocation).
+
+    Y must be passed in: this call allocates nothing, not even through torch.
+    """
+    M, K, N = _shapes(X, Wq)
+    _need(X, torch.float16, (M, K), "X")
+    _need(Y, torch.float16, (M, N), "Y")
+    st = _lib.load().llmint8_matmul_noalloc(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW),
+                                            _ptr(Wq16), _ptr(W16), _ptr(Y), _stream(stream))
+    _check(st, "llmint8_matmul_noalloc")
+    return Y
+
+
 def llmint8_device_status(workspace, stream=None) -> int:
     """Synchronize and read (then clear) the device error word; returns a status code."""
     return int(_lib.load().llmint8_device_status(_ptr(workspace), _stream(stream)))

@@ -491,3 +491,48 @@ llmint8_status llmint8_selftest_timeout(void* workspace, int spin_limit, void* s
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot allocate device memory at the moment they run the matmul:
+// code that executes while a stream is being captured into a CUDA graph (an
+// allocation there is an illegal call that invalidates the capture), callers
+// that must not risk the device-wide synchronization that cudaMalloc/cudaFree
+// may cause inside a latency-critical decode loop, and hosts whose device
+// memory budget is owned by another allocator.  For them the scratch space the
+// matmul needs lives in this file-scope array, sized once at load time; every
+// GPU that loads the library holds it until the process exits.
+// ----------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;  // 8 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+void* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+}  // namespace
+
+extern "C" llmint8_status llmint8_matmul_noalloc(const void* X, int M, int K, int N, float threshold,
+                                                 const int8_t* Wq, const float* colScaleW, const void* Wq16,
+                                                 const void* W16, void* Y, void* stream) {
+    if (!sizes_ok(M, K, N)) return LLMINT8_EINVAL;
+    if (make_layout(M, K, N).total > kNoAllocScratchBytes) return LLMINT8_EWORKSPACE;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = current_device(&dev);
+    if (st != LLMINT8_OK) return st;
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return LLMINT8_ECUDA;
+    void* scratch = nullptr;
+    {
+        // one-time set-up per device, with that device current: host code only
+        // holds a stand-in for the array, so its device address is looked up
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (g_noalloc_ptr[d] == nullptr) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return LLMINT8_ECUDA;
+            g_noalloc_ptr[d] = p;
+        }
+        scratch = g_noalloc_ptr[d];
+    }
+    return llmint8_matmul(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, scratch, kNoAllocScratchBytes,
+                          stream);
+}

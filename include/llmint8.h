@@ -137,6 +137,32 @@ llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold,
                             const float *colScaleW, const void *Wq16, const void *W16, void *Y,
                             void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Allocation-free variant of llmint8_matmul.  The pages describe no such call;
+ * it exists for callers that cannot allocate device memory when they run the
+ * matmul: code running while a stream is captured into a CUDA graph (an
+ * allocation there invalidates the capture), latency-critical loops that must
+ * not risk the device-wide synchronization of cudaMalloc/cudaFree, and hosts
+ * whose device memory is owned by another allocator.
+ *
+ * Same arguments and results as llmint8_matmul minus the workspace: the scratch
+ * space is a static 8 MiB device array inside the library (held by every GPU
+ * that loads it until the process exits).  The call allocates nothing.
+ *   - Shapes whose llmint8_workspace_bytes(M, K, N) exceeds 8 MiB return
+ *     LLMINT8_EWORKSPACE (the 7B-like decode shapes need well under 1 MiB).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents; every
+ *     call resets the parts that must start at zero.  Calls whose work overlaps
+ *     on the GPU (other streams, other host threads without ordering) race on
+ *     it: order them.
+ *   - The device error word lives in the array and is not readable through
+ *     llmint8_device_status.
+ */
+llmint8_status llmint8_matmul_noalloc(const void *X, int M, int K, int N, float threshold,
+                                      const int8_t *Wq, const float *colScaleW, const void *Wq16,
+                                      const void *W16, void *Y, void *stream);
+
 /* ----------------------------------------------------------------------------
  * Introspection (tests and diagnostics; not on the hot path)
  * ------------------------------------------------------------------------- */

@@ -106,6 +106,15 @@ def test_quantize_weight_argument_errors(lib):
     assert lib.llmint8_quantize_weight(P(FAKE), 64, 64, P(FAKE + 4), P(FAKE), None, None) == _lib.EALIGN
 
 
+def test_noalloc_argument_errors(lib):
+    P = ctypes.c_void_p
+    # shapes whose workspace exceeds the static 8 MiB scratch are rejected on the host
+    assert lib.llmint8_matmul_noalloc(P(FAKE), 4096, 8192, 8192, 6.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                      P(FAKE), None) == _lib.EWORKSPACE
+    assert lib.llmint8_matmul_noalloc(P(FAKE), 0, 64, 64, 6.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                      P(FAKE), None) == _lib.EINVAL
+
+
 def test_selftest_argument_errors(lib):
     P = ctypes.c_void_p
     assert lib.llmint8_selftest_timeout(P(0), 10, None) == _lib.EINVAL
