@@ -202,16 +202,26 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------------------- our arm
 
-def traffic_record(kernel_file):
-    """Per-launch DRAM bytes from the committed ncu summary, valid only while the
-    kernel source is unchanged (hash match); else None."""
+KERNEL_SOURCES = {  # the sources each timed kernel is compiled from
+    "k_gemv_decode": ("gemv.cuh", "common.cuh"),
+}
+
+
+def kernel_source_hash(kernel):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "bit_quantization_matmul_row_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary
+    (profiles/traffic.json), valid only while the kernel's sources are unchanged
+    (hash match); else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "bit_quantization_matmul_row_b300", "csrc", kernel_file)
     try:
-        d = json.load(open(p))
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        rec = d.get(kernel_file)
-        if rec and rec.get("source_sha256_16") == h:
+        rec = json.load(open(p)).get(kernel)
+        if rec and rec.get("source_sha256_16") == kernel_source_hash(kernel):
             return rec
     except Exception:
         pass
@@ -260,6 +270,12 @@ def run_ours(args, world, rank, local):
     weight_set = sum(d["c"].K * d["c"].N for d in cases[:3])  # distinct (K,N) weights, one replica
 
     ncase = len(cases)
+    # kernels per call (outlier scan, row quantization, GEMV) as the library plans them
+    for d in cases:
+        c = d["c"]
+        d["kpc"] = api.llmint8_kernels_per_call(c.M, c.K, c.N, c.threshold)
+        d["kernel"] = "k_gemv_decode"
+    launches_per_step = sum(d["kpc"] for d in cases)
 
     # ---- one CUDA graph per step (the 9 llmint8_matmul calls), so the GPU is not
     # starved by host launch latency.  Inside a call the kernels overlap through
@@ -272,7 +288,7 @@ def run_ours(args, world, rank, local):
             for ci, d in enumerate(cases):
                 c = d["c"]
                 Wq, sw, Wd = d["reps"][(gi * ncase + ci) % R]
-                if instrumented:  # xpass, [event], GEMM stage, [event]
+                if instrumented:  # xpass, [event], GEMV, [event]
                     api.llmint8_xpass(d["Xd"], c.threshold, c.N, d["ws"])
                     evs[ci][0].record()
                     api.llmint8_gemm(d["Xd"], c.threshold, Wq, sw, None, Wd, d["Y"], d["ws"])
@@ -305,8 +321,8 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     elapsed_ms = ev_a.elapsed_time(ev_b)
     del graphs
-    # dominant kernel: the same steps with event nodes around every GEMM stage
-    # (this separates the GEMV from the X pass, so it runs without their overlap)
+    # dominant kernel: the same steps with event nodes around every GEMV (this
+    # separates the GEMV from its X pass, so it runs without their overlap)
     G = min(args.steps, args.max_graphs, 64)
     igraphs = [capture(gi, True) for gi in range(G)]
     for i in range(args.warmup):
@@ -326,13 +342,23 @@ def run_ours(args, world, rank, local):
         elapsed_ms = float(t.item())
     total_bytes = step_bytes * args.steps * world
     value = total_bytes / (elapsed_ms * 1e-3) / 1e9
-    gemv_total_ms = sum(sum(r) for r in gemv_ms)
-    gemv_launches = G * ncase
-    achieved = step_bytes * G / (gemv_total_ms * 1e-3) / 1e9
-    per_shape = [{"M": d["c"].M, "K": d["c"].K, "N": d["c"].N, "outliers": d["n_o"],
-                  "gemv_us": 1e3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G,
-                  "gemv_gbs": d["bytes"] / (1e-3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G) / 1e9}
+    per_shape = [{"M": d["c"].M, "K": d["c"].K, "N": d["c"].N, "outliers": d["n_o"], "kernel": d["kernel"],
+                  "kernel_us": 1e3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G,
+                  "kernel_gbs": d["bytes"] / (1e-3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G) / 1e9}
                  for ci, d in enumerate(cases)]
+    by_kernel = {}
+    for ci, d in enumerate(cases):
+        k = by_kernel.setdefault(d["kernel"], {"ms": 0.0, "bytes": 0, "launches": 0})
+        k["ms"] += sum(gemv_ms[gi][ci] for gi in range(G))
+        k["bytes"] += d["bytes"] * G
+        k["launches"] += G
+    dom = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
+    all_ms = sum(k["ms"] for k in by_kernel.values())
+    kernels = {k: {"launches_timed": v["launches"], "launch_us_avg": 1e3 * v["ms"] / v["launches"],
+                   "alg_bytes_per_launch": v["bytes"] / v["launches"],
+                   "achieved_gbs": v["bytes"] / (v["ms"] * 1e-3) / 1e9, "time_share": v["ms"] / all_ms}
+               for k, v in by_kernel.items()}
+    achieved = kernels[dom]["achieved_gbs"]
     time.sleep(0.1)
 
     # ---- end to end through the public call: pinned host X -> device,
@@ -396,7 +422,7 @@ def run_ours(args, world, rank, local):
             cpu = {"value": b / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                    "sample": f"the 9 decode calls of one step, repeated {reps}x ({t:.1f} s of oracle time; "
                              f"A1..A5 per call, weights quantized beforehand)"}
-        trec = traffic_record("gemv.cuh")
+        trec = traffic_record(dom)
         traffic = None if trec is None else trec["dram_bytes_per_launch"]
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -408,17 +434,20 @@ def run_ours(args, world, rank, local):
                               f"after >= {(R - 1) * weight_set / 2**20:.0f} MB of other weights (L2 126 MB)"),
                        "outliers_per_call": [d["n_o"] for d in cases], "bytes_per_step": step_bytes},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "k_gemv_decode",
-                         "alg_bytes_per_launch": step_bytes / ncase,
-                         "launch_us_avg": 1e3 * gemv_total_ms / gemv_launches, "launches_timed": gemv_launches,
-                         "timing": "CUDA events around each GEMV launch in captured steps (GEMV not overlapped "
-                                   "with the X pass); the step value runs the same calls without those events",
-                         "peak_source": f"{peak_src} hbm_gbs (copy, burst)", "per_shape": per_shape},
+                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": dom,
+                         "alg_bytes_per_launch": kernels[dom]["alg_bytes_per_launch"],
+                         "launch_us_avg": kernels[dom]["launch_us_avg"],
+                         "launches_timed": kernels[dom]["launches_timed"],
+                         "timing": "CUDA events around each GEMV launch in captured steps (the GEMV is not "
+                                   "overlapped with its X pass there); the step value runs the same calls without "
+                                   "those events",
+                         "peak_source": f"{peak_src} hbm_gbs (copy, burst)", "kernels": kernels,
+                         "per_shape": per_shape},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "mode": "eager: each call issued from Python through the public llmint8_matmul",
                     "graph_value": e2e_graph_value},
-            "gpu_launches": args.steps * ncase * 3,
+            "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
         }
         if prefill is not None:

@@ -23,6 +23,7 @@ EXPORTS = (
     "llmint8_xpass",
     "llmint8_gemm",
     "llmint8_matmul_noalloc",
+    "llmint8_kernels_per_call",
     "llmint8_workspace_layout",
     "llmint8_device_status",
     "llmint8_selftest_timeout",
@@ -55,6 +56,8 @@ def load() -> ctypes.CDLL:
         lib.llmint8_xpass.argtypes = [P, I, I, I, F, P, Z, P]
         lib.llmint8_gemm.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_noalloc.argtypes = [P, I, I, I, F, P, P, P, P, P, P]
+        lib.llmint8_kernels_per_call.argtypes = [I, I, I, F, I]
+        lib.llmint8_kernels_per_call.restype = I
         lib.llmint8_workspace_layout.argtypes = [I, I, I, ctypes.POINTER(Z)]
         lib.llmint8_device_status.argtypes = [P, P]
         lib.llmint8_selftest_timeout.argtypes = [P, I, P]

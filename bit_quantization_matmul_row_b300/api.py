@@ -51,6 +51,14 @@ def llmint8_workspace_bytes(M: int, K: int, N: int) -> int:
     return int(_lib.load().llmint8_workspace_bytes(int(M), int(K), int(N)))
 
 
+def llmint8_kernels_per_call(M: int, K: int, N: int, threshold: float, write_i32: bool = False) -> int:
+    """Kernels one llmint8_matmul (or, with write_i32, llmint8_matmul_i32) call launches."""
+    n = _lib.load().llmint8_kernels_per_call(M, K, N, float(threshold), 1 if write_i32 else 0)
+    if n < 0:
+        raise LLMInt8Error(f"llmint8_kernels_per_call: invalid arguments M={M} K={K} N={N} t={threshold}")
+    return n
+
+
 def llmint8_workspace_layout(M: int, K: int, N: int) -> dict:
     off = (ctypes.c_size_t * len(_lib.WS_FIELDS))()
     _check(_lib.load().llmint8_workspace_layout(int(M), int(K), int(N), off), "llmint8_workspace_layout")

@@ -275,26 +275,24 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         {
             std::lock_guard<std::mutex> lock(g_mu);
             if (!dev->gemv_attr_set) {
-                const int sm = (int)kGemvDynSmem;
-                if (cudaFuncSetAttribute(k_gemv_decode<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=
-                        cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=
-                        cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=
-                        cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) !=
-                        cudaSuccess)
+                if (cudaFuncSetAttribute(k_gemv_decode<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)gemv_dyn_smem(1)) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)gemv_dyn_smem(1)) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)gemv_dyn_smem(2)) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)gemv_dyn_smem(2)) != cudaSuccess)
                     return LLMINT8_ECUDA;
                 dev->gemv_attr_set = true;
             }
         }
         const dim3 grid(N / kGemvCols), block(kGemvWarps * 32);
-        const size_t dyn = kGemvDynSmem;
         if (M <= 8)
-            return write_i32 ? launch(k_gemv_decode<1, true>, grid, block, dyn, s, true, ga)
-                             : launch(k_gemv_decode<1, false>, grid, block, dyn, s, true, ga);
-        return write_i32 ? launch(k_gemv_decode<2, true>, grid, block, dyn, s, true, ga)
-                         : launch(k_gemv_decode<2, false>, grid, block, dyn, s, true, ga);
+            return write_i32 ? launch(k_gemv_decode<1, true>, grid, block, gemv_dyn_smem(1), s, true, ga)
+                             : launch(k_gemv_decode<1, false>, grid, block, gemv_dyn_smem(1), s, true, ga);
+        return write_i32 ? launch(k_gemv_decode<2, true>, grid, block, gemv_dyn_smem(2), s, true, ga)
+                         : launch(k_gemv_decode<2, false>, grid, block, gemv_dyn_smem(2), s, true, ga);
     }
 
     // A4 operand: gathered, transposed outlier rows of W16
@@ -338,6 +336,15 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         return launch(k_gemm_tc<true>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo, tm_wo,
                       ga);
     return launch(k_gemm_tc<false>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo, tm_wo, ga);
+}
+
+// Kernels one matmul call launches (the plan matmul_impl follows).
+int kernels_per_call(int M, int K, int N, float threshold, bool write_i32) {
+    const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
+    int n = (use_outliers ? 1 : 0) + 1 + 1;  // scan, row quant, GEMV / GEMM
+    if (M > LLMINT8_DECODE_MAX_M && use_outliers && !write_i32) n += 1;  // outlier rows of W16 for the GEMM
+    (void)N;
+    return n;
 }
 
 llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
@@ -457,6 +464,11 @@ llmint8_status llmint8_gemm(const void* X, int M, int K, int N, float threshold,
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
     return gemm_launch(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, L, dev,
                        static_cast<cudaStream_t>(stream));
+}
+
+int llmint8_kernels_per_call(int M, int K, int N, float threshold, int write_i32) {
+    if (!sizes_ok(M, K, N) || std::isnan(threshold)) return -1;
+    return kernels_per_call(M, K, N, threshold, write_i32 != 0);
 }
 
 llmint8_status llmint8_workspace_layout(int M, int K, int N, size_t* offsets) {

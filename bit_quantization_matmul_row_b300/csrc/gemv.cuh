@@ -8,18 +8,23 @@
 // 16 rows it is the limit near 70 % of the HBM roofline.
 //
 // Streaming: one CTA per 16 output columns, K split over 8 warps.  Each warp
-// keeps kGemvRing steps of 1 KB (16 weight rows x 64 K) in flight through a
-// private shared-memory ring filled with cp.async; each thread copies, and
-// later reads back, its own 32 bytes of a step, so the ring needs no
-// cross-thread synchronization.  With two CTAs per SM that is ~128 KB per SM:
-// most of the matrix of the smaller decode shapes is requested at kernel start.
-// The copies are issued before griddepcontrol.wait (the weights do not depend
-// on the X pass), so they overlap the X pass when launched with programmatic
-// dependent launch.
+// keeps gemv_ring(MT) steps in flight through a private shared-memory ring
+// filled with cp.async.  A ring slot holds one step of both operands: 1 KB of
+// weights (16 rows x 64 K) and the matching 16-byte fragments of the X codes
+// (64 K x up to 16 rows), so the codes, which sit in L2, get the same
+// lookahead as the weights: an L2 hit takes over a microsecond while HBM
+// streams at full rate, far longer than a few steps of compute.  Each thread
+// copies, and later reads back, its own bytes of a slot, so the ring needs no
+// cross-thread synchronization.  The weight halves of the first slots are
+// requested before griddepcontrol.wait (weights do not depend on the X pass),
+// so they overlap the X pass under programmatic dependent launch; the code
+// halves follow right after the wait.
 //
-// Epilogue: the 8 warps' int32 partials are summed in shared memory; the CTA
-// adds the fp16 outlier slice (A4, fp32 accumulation, operands prefetched to
-// shared memory) and applies the scale outer product (A5).
+// Epilogue: the 8 warps' int32 partials are summed in shared memory (each
+// warp's drained ring); the CTA adds the fp16 outlier slice (A4, fp32
+// accumulation, operands staged in shared memory while the weights stream) and
+// applies the scale outer product (A5).  Everything the epilogue reads from
+// global memory is requested at kernel start.
 #pragma once
 
 #include "common.cuh"
@@ -30,8 +35,15 @@ namespace llmint8 {
 constexpr int kGemvWarps = 8;
 constexpr int kGemvCols = 16;
 constexpr int kGemvOutChunk = 256;  // outlier columns staged in shared memory at a time
-constexpr int kGemvRing = 8;        // weight steps in flight per warp (1 KB each)
-constexpr size_t kGemvDynSmem = (size_t)kGemvWarps * kGemvRing * 1024;
+
+// Ring of one warp: steps in flight and bytes per step (weights + X code
+// fragments of MT 8-row tiles).  Both rings take 80-84 KB per CTA, so two CTAs
+// fit on an SM next to the static staging buffers.
+__host__ __device__ constexpr int gemv_ring(int mt) { return mt == 1 ? 7 : 5; }
+__host__ __device__ constexpr int gemv_slot(int mt) { return 1024 + 512 * mt; }
+__host__ __device__ constexpr size_t gemv_dyn_smem(int mt) {
+    return (size_t)kGemvWarps * gemv_ring(mt) * gemv_slot(mt);
+}
 
 struct GemvArgs {
     const int8_t* codes;        // [M, K] int8 codes of X
@@ -66,14 +78,22 @@ __device__ __forceinline__ void imma_16832(int (&d)[4], uint32_t a0, uint32_t a1
 // holds 16 contiguous bytes of weight rows n0+g and n0+g+8 at k = kb + 16q, and
 // 16 bytes of X row g (+8) at the same k.  MMA j (0, 1) takes bytes 8j..8j+7 of
 // each: the first word as the k-slot 4q..4q+3 fragment, the second as 16+4q..
+//
+// Ring slot of step s (thread-private bytes at lane * 16):
+//   [0, 512) weight row n0+g, [512, 1024) weight row n0+g+8,
+//   [1024 + 512 t, ...) X codes of row g + 8t.
+// Commit groups: one per weight step before the wait (R), the X halves of those
+// R steps (one group), the outlier staging (one group), then one group per
+// refilled step.
 template <int MT, bool WRITE_I32>
 __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) {
-    __shared__ int32_t s_red[kGemvWarps][16][kGemvCols];                // [warp][x row][column]
+    constexpr int R = gemv_ring(MT);
+    constexpr int SLOT = gemv_slot(MT);
     __shared__ __align__(16) __half s_w16o[kGemvOutChunk][kGemvCols];  // W16[O[j], n0..n0+15]
     __shared__ __align__(16) __half s_xo[16][kGemvOutChunk];           // X[i, O[j]]
     extern __shared__ __align__(16) uint8_t s_ring_all[];
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tq = lane & 3;
     const int n0 = blockIdx.x * kGemvCols;
     const int K = a.K;
@@ -91,115 +111,125 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
         xok[t] = i < a.M;
         xp[t] = a.codes + (size_t)(xok[t] ? i : 0) * K + kb0 + 16 * tq;
     }
+    uint8_t* ring = s_ring_all + (size_t)warp * R * SLOT;
+    auto slot_of = [&](int sn) { return ring + (sn % R) * SLOT + lane * 16; };
+    auto step_ok = [&](int sn) { return sn < nsteps && kb0 + sn * 64 + 16 * tq < kend; };
+    auto issue_w = [&](int sn) {
+        if (step_ok(sn)) {
+            uint8_t* slot = slot_of(sn);
+            cp_async16(slot, w0p + sn * 64);
+            cp_async16(slot + 512, w1p + sn * 64);
+        }
+    };
+    auto issue_x = [&](int sn) {
+        if (step_ok(sn)) {
+            uint8_t* slot = slot_of(sn);
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+                if (xok[t]) cp_async16(slot + 1024 + 512 * t, xp[t] + sn * 64);
+        }
+    };
+
+    // epilogue thread mapping: (row ri, column n0 + nl)
+    const int nl = tid & 15, ri = tid >> 4;
+    const bool active = ri < a.M;
+    const int n = n0 + nl;
+    // constant inputs may be read before the wait
+    const float cs = WRITE_I32 ? 0.0f : a.col_scale[n];
+    pdl_trigger();
+#pragma unroll
+    for (int d = 0; d < R; ++d) {
+        issue_w(d);
+        cp_async_commit();
+    }
+    pdl_wait();
+#pragma unroll
+    for (int d = 0; d < R; ++d) issue_x(d);
+    cp_async_commit();
+    const float rs = (!WRITE_I32 && active) ? __ldcg(a.row_scale + ri) : 0.0f;
+
+    // A4 operands of this CTA's 16 columns for outlier positions [base, base + c):
+    // the W16 rows (32 bytes each) and the gathered X values.  The index loads do
+    // not wait for the count: positions past it are loaded but not used.
+    const int cnt = (!WRITE_I32 && a.use_outliers) ? __ldcg(&a.hdr->outlier_count) : 0;
+    const int nidx = min(K, kGemvOutChunk);
+    auto stage_outliers = [&](int base, int c) {
+        for (int e = tid; e < 2 * nidx; e += kGemvWarps * 32) {
+            const int j = e >> 1, hv = e & 1;
+            const int k = base + j < K ? __ldcg(a.outlier_idx + base + j) : 0;
+            if (j < c) cp_async16(&s_w16o[j][hv * 8], a.W16 + (size_t)k * a.N + n0 + hv * 8);
+        }
+        const int cv = (c + 7) >> 3;
+        for (int e = tid; e < a.M * (kGemvOutChunk / 8); e += kGemvWarps * 32) {
+            const int i = e / (kGemvOutChunk / 8), qv = e - i * (kGemvOutChunk / 8);
+            if (qv < cv) cp_async16(&s_xo[i][qv * 8], a.xo + (size_t)i * a.xo_pitch + base + qv * 8);
+        }
+        cp_async_commit();
+    };
+    if (cnt > 0)
+        stage_outliers(0, min(cnt, kGemvOutChunk));
+    else
+        cp_async_commit();  // keep the group count fixed
+
     int acc[MT][4];
 #pragma unroll
     for (int t = 0; t < MT; ++t)
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[t][r] = 0;
-
-    uint8_t* ring = s_ring_all + (size_t)warp * kGemvRing * 1024;
     const uint4 z = make_uint4(0, 0, 0, 0);
-    auto step_ok = [&](int sn) { return sn < nsteps && kb0 + sn * 64 + 16 * tq < kend; };
-    auto issue_w = [&](int sn) {  // one commit group per step, empty past the end
-        if (step_ok(sn)) {
-            uint8_t* slot = ring + (sn % kGemvRing) * 1024 + lane * 16;
-            cp_async16(slot, w0p + sn * 64);
-            cp_async16(slot + 512, w1p + sn * 64);
+    for (int s = 0; s < nsteps; ++s) {
+        if (s == 0)
+            cp_async_wait_group<1>();      // the first R steps, both halves (staging may be pending)
+        else if (s >= R)
+            cp_async_wait_group<R - 1>();  // the refill of step s was committed R - 1 groups ago
+        const uint8_t* slot = slot_of(s);
+        const uint4 w0 = *reinterpret_cast<const uint4*>(slot);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(slot + 512);
+        const bool ok = step_ok(s);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            const uint4 xf = (ok && xok[t]) ? *reinterpret_cast<const uint4*>(slot + 1024 + 512 * t) : z;
+            imma_16832(acc[t], w0.x, w1.x, w0.y, w1.y, xf.x, xf.y);
+            imma_16832(acc[t], w0.z, w1.z, w0.w, w1.w, xf.z, xf.w);
         }
+        // the slot's values were consumed by the MMAs above: refill it
+        issue_w(s + R);
+        issue_x(s + R);
         cp_async_commit();
-    };
-    constexpr int DX = 4;  // X fragments in flight (steps)
-    uint4 xr[DX][MT];
-    auto load_x = [&](int sn, uint4 (&x)[MT]) {
-        const bool ok = step_ok(sn);
-#pragma unroll
-        for (int t = 0; t < MT; ++t) x[t] = (ok && xok[t]) ? ldg_cg_v4(xp[t] + sn * 64) : z;
-    };
-
-    // Weights are constant inputs: request them before waiting for the X pass,
-    // whose codes, scales and outlier list are read only after pdl_wait().
-    pdl_trigger();
-#pragma unroll
-    for (int d = 0; d < kGemvRing; ++d) issue_w(d);
-    pdl_wait();
-#pragma unroll
-    for (int d = 0; d < DX; ++d) load_x(d, xr[d]);
-
-    // A4 operands of this CTA's 16 columns, copied to shared memory while the
-    // weights stream: the outlier rows of W16 (32 bytes each) and the gathered
-    // outlier values of X (one more commit group).
-    const int cnt = (!WRITE_I32 && a.use_outliers) ? __ldcg(&a.hdr->outlier_count) : 0;
-    auto stage_outliers = [&](int base, int c) {
-        for (int e = threadIdx.x; e < 2 * c; e += kGemvWarps * 32) {
-            const int j = e >> 1, hv = e & 1;
-            const int k = __ldcg(a.outlier_idx + base + j);
-            cp_async16(&s_w16o[j][hv * 8], a.W16 + (size_t)k * a.N + n0 + hv * 8);
-        }
-        const int cv = (c + 7) >> 3;
-        for (int e = threadIdx.x; e < a.M * cv; e += kGemvWarps * 32) {
-            const int i = e / cv, qv = e - i * cv;
-            cp_async16(&s_xo[i][qv * 8], a.xo + (size_t)i * a.xo_pitch + base + qv * 8);
-        }
-        cp_async_commit();
-    };
-    if (cnt > 0) stage_outliers(0, min(cnt, kGemvOutChunk));
-
-    for (int s0 = 0; s0 < nsteps; s0 += DX) {
-#pragma unroll
-        for (int d = 0; d < DX; ++d) {
-            const int s = s0 + d;
-            if (s < nsteps) {
-                // every group older than the newest kGemvRing-1 is complete: step s has landed
-                cp_async_wait_group<kGemvRing - 1>();
-                const uint8_t* slot = ring + (s % kGemvRing) * 1024 + lane * 16;
-                const uint4 w0 = *reinterpret_cast<const uint4*>(slot);
-                const uint4 w1 = *reinterpret_cast<const uint4*>(slot + 512);
-                uint4 xf[MT];
-#pragma unroll
-                for (int t = 0; t < MT; ++t) xf[t] = xr[d][t];
-                load_x(s + DX, xr[d]);
-#pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    imma_16832(acc[t], w0.x, w1.x, w0.y, w1.y, xf[t].x, xf[t].y);
-                    imma_16832(acc[t], w0.z, w1.z, w0.w, w1.w, xf[t].z, xf[t].w);
-                }
-                // the slot's values were consumed by the MMAs above: refill it
-                issue_w(s + kGemvRing);
-            }
-        }
     }
 
+    // No copy may still target shared memory: the ring is drained (its later
+    // groups are empty) and the staging group has landed.  Each warp's partials
+    // then go to its own ring, [16 x rows][16 columns] int32.
+    cp_async_wait_all();
+    int32_t* red = reinterpret_cast<int32_t*>(ring);
     // accumulator layout: d0,d1 -> (column g, x rows 8t+2q, +1); d2,d3 -> (column g+8, same rows)
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
         const int i0 = 8 * t + 2 * tq;
-        s_red[warp][i0][g] = acc[t][0];
-        s_red[warp][i0 + 1][g] = acc[t][1];
-        s_red[warp][i0][g + 8] = acc[t][2];
-        s_red[warp][i0 + 1][g + 8] = acc[t][3];
+        red[i0 * kGemvCols + g] = acc[t][0];
+        red[(i0 + 1) * kGemvCols + g] = acc[t][1];
+        red[i0 * kGemvCols + g + 8] = acc[t][2];
+        red[(i0 + 1) * kGemvCols + g + 8] = acc[t][3];
     }
     __syncthreads();
 
-    const int nl = threadIdx.x & 15, i = threadIdx.x >> 4;
-    const bool active = i < a.M;
-    const int n = n0 + nl;
     int32_t c = 0;
     if (active) {
 #pragma unroll
-        for (int w = 0; w < kGemvWarps; ++w) c += s_red[w][i][nl];
+        for (int w = 0; w < kGemvWarps; ++w)
+            c += reinterpret_cast<const int32_t*>(s_ring_all + (size_t)w * R * SLOT)[ri * kGemvCols + nl];
     }
-    cp_async_wait_all();  // no copy may still target shared memory when the CTA ends
     if (WRITE_I32) {
-        if (active) reinterpret_cast<int32_t*>(a.out)[(size_t)i * a.N + n] = c;
+        if (active) reinterpret_cast<int32_t*>(a.out)[(size_t)ri * a.N + n] = c;
         return;
     }
     float f = 0.0f;
     if (cnt > 0) {
-        __syncthreads();
         for (int base = 0;;) {
             const int cc = min(kGemvOutChunk, cnt - base);
             if (active)
-                for (int j = 0; j < cc; ++j) f = fmaf(__half2float(s_xo[i][j]), __half2float(s_w16o[j][nl]), f);
+                for (int j = 0; j < cc; ++j) f = fmaf(__half2float(s_xo[ri][j]), __half2float(s_w16o[j][nl]), f);
             base += kGemvOutChunk;
             if (base >= cnt) break;
             __syncthreads();
@@ -209,8 +239,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
         }
     }
     if (active) {
-        const float scale = __ldcg(a.row_scale + i) * a.col_scale[n] * (1.0f / 16129.0f);
-        reinterpret_cast<__half*>(a.out)[(size_t)i * a.N + n] = __float2half_rn(fmaf((float)c, scale, f));
+        const float scale = rs * cs * (1.0f / 16129.0f);
+        reinterpret_cast<__half*>(a.out)[(size_t)ri * a.N + n] = __float2half_rn(fmaf((float)c, scale, f));
     }
 }
 

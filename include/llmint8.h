@@ -180,6 +180,16 @@ llmint8_status llmint8_matmul_i32(const void *X, int M, int K, int N, float thre
                                   int32_t *C, void *workspace, size_t workspace_bytes,
                                   void *stream);
 
+/*
+ * Number of kernels one llmint8_matmul (write_i32 = 0) or llmint8_matmul_i32
+ * (write_i32 = 1) call launches for this shape and threshold (pass +INFINITY
+ * for llmint8_matmul_int8): the outlier scan (not run at +INFINITY), the row
+ * quantization, for M > 16 with a finite threshold and write_i32 = 0 the
+ * gather of the outlier rows of W16, and the GEMV or GEMM.  -1 for arguments
+ * the call would reject as EINVAL.  Host-only; touches no device.
+ */
+int llmint8_kernels_per_call(int M, int K, int N, float threshold, int write_i32);
+
 /* Workspace fields whose offsets llmint8_workspace_layout reports. */
 enum {
     LLMINT8_WS_STATUS = 0,       /* uint32: device error word (0 = OK, else an llmint8_status) */

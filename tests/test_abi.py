@@ -120,3 +120,19 @@ def test_selftest_argument_errors(lib):
     assert lib.llmint8_selftest_timeout(P(0), 10, None) == _lib.EINVAL
     assert lib.llmint8_selftest_timeout(P(FAKE), 0, None) == _lib.EINVAL
     assert lib.llmint8_selftest_timeout(P(FAKE), 10 ** 8, None) == _lib.EINVAL
+
+
+def test_kernels_per_call(lib):
+    inf = float("inf")
+    k = lib.llmint8_kernels_per_call
+    # decode: outlier scan + row quantization + GEMV (no scan without outliers)
+    for M, K in ((1, 16), (1, 16384), (4, 4096), (9, 64), (16, 65536)):
+        assert k(M, K, 4096, 6.0, 0) == 3, (M, K)
+        assert k(M, K, 4096, 6.0, 1) == 3
+        assert k(M, K, 4096, inf, 0) == 2
+    # prefill: scan + row quantization + outlier rows of W16 + GEMM
+    assert k(17, 4096, 4096, 6.0, 0) == 4
+    assert k(17, 4096, 4096, 6.0, 1) == 3       # the int32 result leaves out the fp16 slice
+    assert k(17, 4096, 4096, inf, 0) == 2
+    assert k(0, 64, 64, 6.0, 0) == -1
+    assert k(1, 64, 64, math.nan, 0) == -1

@@ -47,6 +47,23 @@ def test_decode_ragged(M):
     check(X, W, 6.0)
 
 
+@pytest.mark.parametrize("M,K,N", [(1, 16384, 272), (2, 8192, 144), (5, 2048, 400), (16, 65536, 32)])
+def test_decode_long_k(M, K, N):
+    # long rows: many 64-wide steps per warp (ring wrap-around), K = 65536 is the
+    # largest accepted (|C| up to 127^2 * 65536 < 2^31)
+    X, W = xw(M, K, N, frac=0.01, seed=M * K, min_count=3)
+    check(X, W, 6.0)
+
+
+@pytest.mark.parametrize("M,frac", [(1, 0.3), (4, 0.45), (16, 0.4)])
+def test_decode_outlier_chunks(M, frac):
+    # 300-500 outlier columns: more than one 256-column chunk of the fp16 slice
+    # in the GEMV epilogue, the last one partial
+    X, W = xw(M, 1040, 144, frac=frac, seed=M + 700)
+    g, ref = check(X, W, 6.0)
+    assert 256 < len(g["outliers"]) < 512
+
+
 @pytest.mark.parametrize("M,K,N", [(17, 64, 256), (130, 272, 272), (300, 1088, 400), (256, 2112, 512)])
 def test_prefill_ragged(M, K, N):
     # ragged M tiles, ragged N tiles (N % 256 != 0), K not a multiple of 64,
@@ -83,7 +100,39 @@ def test_negative_threshold(M):
     assert not g["s_x"].any()
 
 
-@pytest.mark.parametrize("M", [16, 256])
+@pytest.mark.parametrize("M", [1, 4, 16, 64])
+def test_rounding_ties_go_away_from_zero(M):
+    # Row absmax 127 makes the scale factor exactly 1, so x = k + 1/2 are exact
+    # ties of the code rounding: they must go away from zero (decode path for
+    # M = 1, 4, 16; tensor-core path for 64).
+    K, N = 1024, 64
+    rng = np.random.default_rng(M)
+    X = (rng.integers(-127, 127, size=(M, K)) + 0.5).astype(np.float16)
+    X[:, 0] = 127
+    W, _ = synthetic.make_w(K, N, seed=M)
+    g, ref = check(X, W, 200.0)
+    x = X.astype(np.float64)
+    expect = (np.sign(x) * np.floor(np.abs(x) + 0.5)).astype(np.int8)
+    assert np.array_equal(g["codes"].astype(np.int8), expect)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 200])
+@pytest.mark.parametrize("t", [6.0, 6.001])
+def test_threshold_boundary_values(M, t):
+    # |x| > t is strict: a column whose largest |x| equals t (or is the fp16
+    # value just below a non-representable t) stays in the int8 part; the next
+    # fp16 value above t makes it an outlier column.
+    K, N = 512, 64
+    X, W = xw(M, K, N, frac=0.0, seed=M)
+    at = np.float16(6.0)                      # == t, or just below 6.001
+    above = np.float16(6.00390625)            # next fp16 above 6.0 (and above 6.001)
+    X[M - 1, 10], X[0, 20], X[M // 2, 30] = at, -above, above
+    X[0, 40] = -at
+    g, ref = check(X, W, t)
+    assert set(g["outliers"].tolist()) == {20, 30}
+
+
+@pytest.mark.parametrize("M", [2, 16, 256])
 def test_exactness_beyond_fp32_integer_range(M):
     # All codes +-127 and K = 8192: |C| reaches 127^2 * 8192 = 132,124,672 > 2^24,
     # so any accumulation in plain fp32 beyond 1024 products would round.

@@ -34,7 +34,7 @@ def _noalloc_via_c_abi(X, t, Wq, sw, Wq16, W16, Y):
     return Y
 
 
-@pytest.mark.parametrize("M,K,N", [(16, 4096, 4096), (300, 1088, 400)])
+@pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 4096), (300, 1088, 400)])
 def test_noalloc_matches_workspace_entry_point_two_calls(M, K, N):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
