@@ -276,23 +276,23 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
             std::lock_guard<std::mutex> lock(g_mu);
             if (!dev->gemv_attr_set) {
                 if (cudaFuncSetAttribute(k_gemv_decode<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemv_dyn_smem(1)) != cudaSuccess ||
+                                         (int)gemv_dyn_smem(8)) != cudaSuccess ||
                     cudaFuncSetAttribute(k_gemv_decode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemv_dyn_smem(1)) != cudaSuccess ||
+                                         (int)gemv_dyn_smem(8)) != cudaSuccess ||
                     cudaFuncSetAttribute(k_gemv_decode<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemv_dyn_smem(2)) != cudaSuccess ||
+                                         (int)gemv_dyn_smem(16)) != cudaSuccess ||
                     cudaFuncSetAttribute(k_gemv_decode<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemv_dyn_smem(2)) != cudaSuccess)
+                                         (int)gemv_dyn_smem(16)) != cudaSuccess)
                     return LLMINT8_ECUDA;
                 dev->gemv_attr_set = true;
             }
         }
         const dim3 grid(N / kGemvCols), block(kGemvWarps * 32);
         if (M <= 8)
-            return write_i32 ? launch(k_gemv_decode<1, true>, grid, block, gemv_dyn_smem(1), s, true, ga)
-                             : launch(k_gemv_decode<1, false>, grid, block, gemv_dyn_smem(1), s, true, ga);
-        return write_i32 ? launch(k_gemv_decode<2, true>, grid, block, gemv_dyn_smem(2), s, true, ga)
-                         : launch(k_gemv_decode<2, false>, grid, block, gemv_dyn_smem(2), s, true, ga);
+            return write_i32 ? launch(k_gemv_decode<1, true>, grid, block, gemv_dyn_smem(M), s, true, ga)
+                             : launch(k_gemv_decode<1, false>, grid, block, gemv_dyn_smem(M), s, true, ga);
+        return write_i32 ? launch(k_gemv_decode<2, true>, grid, block, gemv_dyn_smem(M), s, true, ga)
+                         : launch(k_gemv_decode<2, false>, grid, block, gemv_dyn_smem(M), s, true, ga);
     }
 
     // A4 operand: gathered, transposed outlier rows of W16

@@ -34,15 +34,16 @@ namespace llmint8 {
 
 constexpr int kGemvWarps = 8;
 constexpr int kGemvCols = 16;
-constexpr int kGemvOutChunk = 256;  // outlier columns staged in shared memory at a time
+constexpr int kGemvOutChunk = 128;  // outlier columns staged in shared memory at a time
 
-// Ring of one warp: steps in flight and bytes per step (weights + X code
-// fragments of MT 8-row tiles).  Both rings take 80-84 KB per CTA, so two CTAs
-// fit on an SM next to the static staging buffers.
-__host__ __device__ constexpr int gemv_ring(int mt) { return mt == 1 ? 7 : 5; }
-__host__ __device__ constexpr int gemv_slot(int mt) { return 1024 + 512 * mt; }
-__host__ __device__ constexpr size_t gemv_dyn_smem(int mt) {
-    return (size_t)kGemvWarps * gemv_ring(mt) * gemv_slot(mt);
+// Ring of one warp: steps in flight, and bytes per step for M rows of X: 1 KB of
+// weights plus 64 bytes of X codes per row (the 4 threads of a row hold 16
+// bytes each).  The ring takes at most 96 KB per CTA, so two CTAs fit on an SM
+// next to the static staging buffers; 8 steps cover a whole K = 4096 slice.
+__host__ __device__ constexpr int gemv_ring(int mt) { return mt == 1 ? 8 : 6; }
+__host__ __device__ constexpr int gemv_slot(int M) { return 1024 + 64 * M; }
+__host__ __device__ constexpr size_t gemv_dyn_smem(int M) {
+    return (size_t)kGemvWarps * gemv_ring(M <= 8 ? 1 : 2) * gemv_slot(M);
 }
 
 struct GemvArgs {
@@ -81,14 +82,15 @@ __device__ __forceinline__ void imma_16832(int (&d)[4], uint32_t a0, uint32_t a1
 //
 // Ring slot of step s (thread-private bytes at lane * 16):
 //   [0, 512) weight row n0+g, [512, 1024) weight row n0+g+8,
-//   [1024 + 512 t, ...) X codes of row g + 8t.
+//   [1024 + 512 t, ...) X codes of row g + 8t (only rows < M are copied and
+//   read, so the slot is 1024 + 64 M bytes).
 // Commit groups: one per weight step before the wait (R), the X halves of those
 // R steps (one group), the outlier staging (one group), then one group per
 // refilled step.
 template <int MT, bool WRITE_I32>
 __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) {
     constexpr int R = gemv_ring(MT);
-    constexpr int SLOT = gemv_slot(MT);
+    const int SLOT = gemv_slot(a.M);
     __shared__ __align__(16) __half s_w16o[kGemvOutChunk][kGemvCols];  // W16[O[j], n0..n0+15]
     __shared__ __align__(16) __half s_xo[16][kGemvOutChunk];           // X[i, O[j]]
     extern __shared__ __align__(16) uint8_t s_ring_all[];
