@@ -30,6 +30,7 @@ struct DeviceInfo {
     int sms = 0;
     bool gemm_attr_set = false;
     bool gemv_attr_set = false;
+    bool rowq_cluster_attr_set = false;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -148,6 +149,36 @@ int row_quant_vpt(int K) {
     return 0;
 }
 
+// Decode X pass in one clustered row-quantization launch: M <= 16, a finite
+// threshold and rows of at most 4096 columns (two 16-byte vectors per thread).
+bool cluster_flags_apply(int M, int K, float threshold) {
+    const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
+    const int vpt = row_quant_vpt(K);
+    return M <= LLMINT8_DECODE_MAX_M && use_outliers && (vpt == 1 || vpt == 2);
+}
+
+// As launch(), as one thread-block cluster of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+llmint8_status launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                              unsigned cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster_x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? LLMINT8_OK : LLMINT8_ECUDA;
+}
+
+
 // Checks shared by every entry point that runs part of the matmul.
 llmint8_status check_common(const void* X, int M, int K, int N, float threshold, void* workspace, size_t ws_bytes,
                             Layout* L, DeviceInfo** dev) {
@@ -196,7 +227,7 @@ struct WsView {
 
 // A1 + A2 into the workspace.
 llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* workspace, const Layout& L,
-                            const DeviceInfo* dev, cudaStream_t s) {
+                            DeviceInfo* dev, cudaStream_t s) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
     const WsView w(workspace, L);
     const __half* Xh = static_cast<const __half*>(X);
@@ -205,6 +236,10 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
     // A1: outlier columns.  With one row group (always for M <= 64) each scan CTA
     // stores its bitmap words directly and CTA 0 resets the error word; with
     // several row groups the words are OR-ed atomically into a zeroed map.
+    // Short decode rows: the row-quantization CTAs form one cluster and find the
+    // outlier columns themselves (no scan kernel).  Longer rows keep the scan:
+    // its K / 256 CTAs share the flag work that one CTA per row would do alone.
+    const bool cluster = cluster_flags_apply(M, K, threshold);
     const int gx = (K + kScanCols - 1) / kScanCols;
     int gy = 1;
     if (M > 64) {
@@ -213,7 +248,7 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
         if (gy > cap) gy = cap;
         if (gy < 1) gy = 1;
     }
-    if (use_outliers) {
+    if (use_outliers && !cluster) {
         if (gy > 1 && cudaMemsetAsync(static_cast<uint8_t*>(workspace) + L.hdr, 0, L.idx - L.hdr, s) != cudaSuccess)
             return LLMINT8_ECUDA;
         st = launch(k_outlier_scan, dim3(gx, gy), dim3(kScanThreads), 0, s, true, Xh, M, K, threshold, w.bitmap,
@@ -235,8 +270,26 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
     ra.xo = use_outliers ? w.xo : nullptr;
     ra.xo_pitch = L.kp;
     ra.no_outliers = use_outliers ? 0 : 1;
-    ra.clear_status = use_outliers ? 0 : 1;
+    ra.clear_status = (use_outliers && !cluster) ? 0 : 1;
+    ra.t = threshold;
+    ra.cluster_flags = cluster ? 1 : 0;
     const bool pdl = true;
+    if (cluster) {
+        {
+            std::lock_guard<std::mutex> lock(g_mu);
+            if (!dev->rowq_cluster_attr_set) {  // clusters of up to 16 CTAs (M <= 16)
+                if (cudaFuncSetAttribute(k_row_quant<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_row_quant<2>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                        cudaSuccess)
+                    return LLMINT8_ECUDA;
+                dev->rowq_cluster_attr_set = true;
+            }
+        }
+        const unsigned cm = (unsigned)M;
+        return row_quant_vpt(K) == 1 ? launch_cluster(k_row_quant<1>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra)
+                                     : launch_cluster(k_row_quant<2>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra);
+    }
     switch (row_quant_vpt(K)) {
         case 1: return launch(k_row_quant<1>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
         case 2: return launch(k_row_quant<2>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
@@ -341,7 +394,10 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
 // Kernels one matmul call launches (the plan matmul_impl follows).
 int kernels_per_call(int M, int K, int N, float threshold, bool write_i32) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
-    int n = (use_outliers ? 1 : 0) + 1 + 1;  // scan, row quant, GEMV / GEMM
+    // short decode rows find their outlier columns in the row-quantization
+    // cluster: no scan kernel
+    const bool scan = use_outliers && !cluster_flags_apply(M, K, threshold);
+    int n = (scan ? 1 : 0) + 1 + 1;  // scan, row quant, GEMV / GEMM
     if (M > LLMINT8_DECODE_MAX_M && use_outliers && !write_i32) n += 1;  // outlier rows of W16 for the GEMM
     (void)N;
     return n;

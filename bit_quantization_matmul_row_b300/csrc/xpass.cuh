@@ -16,6 +16,8 @@
 // tcgen05 kind).
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace llmint8 {
@@ -113,7 +115,15 @@ struct RowQuantArgs {
     int xo_pitch;             // elements; gathered columns are zero-padded up to a multiple of 64
     int no_outliers;          // threshold +inf: no scan ran, the bit map is not read
     int clear_status;         // no earlier kernel of this call reset the error word
+    float t;                  // outlier threshold (cluster_flags)
+    int cluster_flags;        // launched as one cluster of M CTAs: the outlier columns are
+                              // found here (no scan kernel, the bit map is not read)
 };
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
 // Round half away from zero, then clamp to [-127, 127] (clamp after rounding,
 // before the integer conversion: LLM quantization in practice, section 3.2).
@@ -125,10 +135,21 @@ __device__ __forceinline__ float code_of(float x, float sf) {
 // A2.  One CTA per row.  VPT = 16-byte vectors per thread kept in registers
 // between the absmax pass and the code pass (the row is re-read when K is
 // larger than 256 * 8 * VPT).
+//
+// Decode with short rows (cluster_flags, VPT 1 or 2): the M CTAs form one thread-block cluster and
+// find the outlier columns themselves, without the scan kernel.  Each CTA flags
+// the columns of its own row (already in registers), pushes that bit map into
+// the shared memory of every CTA of the cluster, and after one cluster barrier
+// ORs the M row maps locally (A1: a column is an outlier when any row exceeds t).
 template <int VPT>
 __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
-    __shared__ uint32_t s_bits[kMaxWords];
-    __shared__ int32_t s_prefix[kMaxWords];  // outliers in words before w
+    // bit-map words held in shared memory: the whole row when it sits in registers
+    constexpr int kWords = VPT > 0 ? (VPT * 64 > kRowThreads ? VPT * 64 : kRowThreads) : kMaxWords;
+    constexpr bool kCluster = VPT == 1 || VPT == 2;     // instantiations that serve cluster_flags
+    constexpr int kRowWords = kCluster ? VPT * 64 : 1;  // bit-map words of one row
+    __shared__ uint32_t s_bits[kWords];
+    __shared__ int32_t s_prefix[kWords];  // outliers in words before w
+    __shared__ uint32_t s_rowflags[kCluster ? LLMINT8_DECODE_MAX_M : 1][kRowWords];  // [row][word]
     __shared__ int32_t s_wsum[kRowThreads / 32];
     __shared__ float s_wmax[kRowThreads / 32];
     __shared__ int32_t s_total;
@@ -137,6 +158,10 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
     const int row = blockIdx.x;
     const int K = a.K;
     const int nwords = (K + 31) >> 5;
+    const bool cflags = kCluster && a.cluster_flags;
+    // first half of the barrier that makes sure every CTA of the cluster runs
+    // before any writes into its shared memory
+    if (cflags) cluster_arrive_relaxed();
     pdl_trigger();
     pdl_wait();
 
@@ -152,14 +177,39 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
     }
     if (a.clear_status && row == 0 && tid == 0) a.hdr->status = 0u;
 
+    if (cflags) {
+        namespace cg = cooperative_groups;
+        cg::cluster_group cluster = cg::this_cluster();
+        const unsigned csize = cluster.num_blocks();  // == M, rank == row
+        cluster_wait();
+#pragma unroll
+        for (int i = 0; i < (VPT > 0 ? VPT : 1); ++i) {
+            const int vi = tid + i * kRowThreads;
+            // lanes 4k..4k+3 hold the 4 vectors (32 columns) of bit-map word vi / 4
+            uint32_t word = (vi < nvec ? outlier_mask8(v[i], a.t) : 0u) << (8 * (lane & 3));
+            word |= __shfl_xor_sync(0xffffffffu, word, 1);
+            word |= __shfl_xor_sync(0xffffffffu, word, 2);
+            if ((lane & 3) == 0 && vi < nvec)
+                for (unsigned r = 0; r < csize; ++r) *cluster.map_shared_rank(&s_rowflags[row][vi >> 2], r) = word;
+        }
+        cluster.sync();  // every row's map has landed everywhere; no remote access follows
+    }
+
     // --- bitmap -> shared memory, exclusive prefix of popcounts (block scan) ---
-    constexpr int WPT = kMaxWords / kRowThreads;  // words per thread (8)
+    constexpr int WPT = kWords / kRowThreads;  // words per thread
     int local[WPT];
     int tsum = 0;
 #pragma unroll
     for (int i = 0; i < WPT; ++i) {
         const int w = tid * WPT + i;
-        const uint32_t b = (w < nwords && !a.no_outliers) ? __ldcg(a.bitmap + w) : 0u;
+        uint32_t b = 0u;
+        if (w < nwords && !a.no_outliers) {
+            if (cflags) {
+                for (int r = 0; r < a.M; ++r) b |= s_rowflags[r][w];
+            } else {
+                b = __ldcg(a.bitmap + w);
+            }
+        }
         if (w < nwords) s_bits[w] = b;
         local[i] = __popc(b);
         tsum += local[i];
@@ -267,7 +317,31 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
     if (tid == 0) a.row_scale[row] = amax;
 
     // --- outlier list (block 0) and gathered outlier columns of this row ---
-    if (n_out > 0 && (a.xo != nullptr || row == 0)) {
+    if (VPT > 0 && n_out > 0 && (a.xo != nullptr || row == 0)) {
+        // from the registers that hold the row: each thread places the outliers
+        // of its own vectors
+        __half* xo_row = a.xo ? a.xo + (size_t)row * a.xo_pitch : nullptr;
+#pragma unroll
+        for (int i = 0; i < (VPT > 0 ? VPT : 1); ++i) {
+            const int vi = tid + i * kRowThreads;
+            if (vi < nvec) {
+                const int w = vi >> 2, sh = (vi & 3) * 8;
+                const uint32_t word = s_bits[w];
+                uint32_t b = (word >> sh) & 0xFFu;
+                while (b) {
+                    const int e = __ffs(b) - 1;
+                    b &= b - 1;
+                    const int pos = s_prefix[w] + __popc(word & ((1u << (sh + e)) - 1u));
+                    if (xo_row) {
+                        const uint4 x = v[i];
+                        const uint32_t w32 = (e & 4) ? ((e & 2) ? x.w : x.z) : ((e & 2) ? x.y : x.x);
+                        xo_row[pos] = __ushort_as_half((unsigned short)(w32 >> (16 * (e & 1))));
+                    }
+                    if (row == 0) a.outlier_idx[pos] = 8 * vi + e;
+                }
+            }
+        }
+    } else if (n_out > 0 && (a.xo != nullptr || row == 0)) {
         __half* xo_row = a.xo ? a.xo + (size_t)row * a.xo_pitch : nullptr;
         for (int w = tid; w < nwords; w += kRowThreads) {
             uint32_t b = s_bits[w];

@@ -183,10 +183,12 @@ llmint8_status llmint8_matmul_i32(const void *X, int M, int K, int N, float thre
 /*
  * Number of kernels one llmint8_matmul (write_i32 = 0) or llmint8_matmul_i32
  * (write_i32 = 1) call launches for this shape and threshold (pass +INFINITY
- * for llmint8_matmul_int8): the outlier scan (not run at +INFINITY), the row
- * quantization, for M > 16 with a finite threshold and write_i32 = 0 the
- * gather of the outlier rows of W16, and the GEMV or GEMM.  -1 for arguments
- * the call would reject as EINVAL.  Host-only; touches no device.
+ * for llmint8_matmul_int8): the outlier scan (not run at +INFINITY, nor for
+ * M <= 16 with K <= 4096, where the row-quantization CTAs form one cluster and
+ * find the outlier columns themselves), the row quantization, for M > 16 with a
+ * finite threshold and write_i32 = 0 the gather of the outlier rows of W16, and
+ * the GEMV or GEMM.  -1 for arguments the call would reject as EINVAL.
+ * Host-only; touches no device.
  */
 int llmint8_kernels_per_call(int M, int K, int N, float threshold, int write_i32);
 

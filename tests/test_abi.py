@@ -125,11 +125,16 @@ def test_selftest_argument_errors(lib):
 def test_kernels_per_call(lib):
     inf = float("inf")
     k = lib.llmint8_kernels_per_call
-    # decode: outlier scan + row quantization + GEMV (no scan without outliers)
-    for M, K in ((1, 16), (1, 16384), (4, 4096), (9, 64), (16, 65536)):
-        assert k(M, K, 4096, 6.0, 0) == 3, (M, K)
-        assert k(M, K, 4096, 6.0, 1) == 3
+    # short decode rows (K <= 4096): the row-quantization cluster finds the
+    # outlier columns itself, then the GEMV
+    for M, K in ((1, 16), (1, 4096), (4, 4096), (9, 64), (16, 4096)):
+        assert k(M, K, 4096, 6.0, 0) == 2, (M, K)
+        assert k(M, K, 4096, 6.0, 1) == 2
         assert k(M, K, 4096, inf, 0) == 2
+    # longer decode rows: outlier scan + row quantization + GEMV
+    for M, K in ((1, 4112), (1, 16384), (16, 11008), (16, 65536)):
+        assert k(M, K, 4096, 6.0, 0) == 3, (M, K)
+        assert k(M, K, 4096, inf, 0) == 2       # no outlier scan
     # prefill: scan + row quantization + outlier rows of W16 + GEMM
     assert k(17, 4096, 4096, 6.0, 0) == 4
     assert k(17, 4096, 4096, 6.0, 1) == 3       # the int32 result leaves out the fp16 slice
