@@ -36,6 +36,8 @@ _lib = None
 def load() -> ctypes.CDLL:
     """Load libllmint8.so (built in-tree).  Raises if it has not been built."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib

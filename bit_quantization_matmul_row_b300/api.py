@@ -30,20 +30,25 @@ def _check(status: int, where: str):
         raise LLMInt8Error(status, where)
 
 
+# The per-call path is kept thin: device pointers and the stream handle cross as
+# plain integers (ctypes converts them for the void* arguments).
+
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream=None):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+def _stream(stream=None, like=None):
+    """Raw handle of `stream`, else of the current stream of `like`'s device."""
+    if stream is not None:
+        return stream.cuda_stream
+    dev = like.device.index if like is not None else torch.cuda.current_device()
+    return torch._C._cuda_getCurrentRawStream(dev)
 
 
 def _need(t, dtype, shape, name):
     if t is None:
         return
-    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+    if t.dtype != dtype or t.shape != shape or not t.is_contiguous():
         raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
 
 
@@ -55,7 +60,7 @@ def llmint8_kernels_per_call(M: int, K: int, N: int, threshold: float, write_i32
     """Kernels one llmint8_matmul (or, with write_i32, llmint8_matmul_i32) call launches."""
     n = _lib.load().llmint8_kernels_per_call(M, K, N, float(threshold), 1 if write_i32 else 0)
     if n < 0:
-        raise LLMInt8Error(f"llmint8_kernels_per_call: invalid arguments M={M} K={K} N={N} t={threshold}")
+        raise ValueError(f"llmint8_kernels_per_call: invalid arguments M={M} K={K} N={N} t={threshold}")
     return n
 
 
@@ -87,7 +92,7 @@ def llmint8_quantize_weight(W: torch.Tensor, Wq=None, colScaleW=None, Wq16=None,
     _need(Wq, torch.int8, (N, K), "Wq")
     _need(colScaleW, torch.float32, (N,), "colScaleW")
     _need(Wq16, torch.float16, (N, K), "Wq16")
-    st = _lib.load().llmint8_quantize_weight(_ptr(W), K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Wq16), _stream(stream))
+    st = _lib.load().llmint8_quantize_weight(_ptr(W), K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Wq16), _stream(stream, W))
     _check(st, "llmint8_quantize_weight")
     return Wq, colScaleW, Wq16
 
@@ -108,7 +113,7 @@ def llmint8_matmul(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspace=Non
     _need(X, torch.float16, (M, K), "X")
     _need(Y, torch.float16, (M, N), "Y")
     st = _lib.load().llmint8_matmul(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
-                                    _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream))
+                                    _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul")
     return Y
 
@@ -123,7 +128,7 @@ def llmint8_matmul_int8(X, Wq, colScaleW, Wq16, Y=None, workspace=None, stream=N
     _need(X, torch.float16, (M, K), "X")
     _need(Y, torch.float16, (M, N), "Y")
     st = _lib.load().llmint8_matmul_int8(_ptr(X), M, K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Wq16), _ptr(Y),
-                                         _ptr(workspace), workspace.numel(), _stream(stream))
+                                         _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul_int8")
     return Y
 
@@ -138,7 +143,7 @@ def llmint8_matmul_i32(X, threshold, Wq, colScaleW, Wq16, C=None, workspace=None
     _need(X, torch.float16, (M, K), "X")
     _need(C, torch.int32, (M, N), "C")
     st = _lib.load().llmint8_matmul_i32(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
-                                        _ptr(C), _ptr(workspace), workspace.numel(), _stream(stream))
+                                        _ptr(C), _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul_i32")
     return C
 
@@ -148,7 +153,7 @@ def llmint8_xpass(X, threshold, N, workspace, stream=None):
     M, K = X.shape
     _need(X, torch.float16, (M, K), "X")
     st = _lib.load().llmint8_xpass(_ptr(X), M, K, int(N), float(threshold), _ptr(workspace), workspace.numel(),
-                                   _stream(stream))
+                                   _stream(stream, X))
     _check(st, "llmint8_xpass")
 
 
@@ -157,7 +162,7 @@ def llmint8_gemm(X, threshold, Wq, colScaleW, Wq16, W16, Y, workspace, stream=No
     M, K, N = _shapes(X, Wq)
     _need(Y, torch.float16, (M, N), "Y")
     st = _lib.load().llmint8_gemm(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
-                                  _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream))
+                                  _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_gemm")
     return Y
 
@@ -174,18 +179,18 @@ def llmint8_matmul_noalloc(X, threshold, Wq, colScaleW, Wq16, W16, Y, stream=Non
     _need(X, torch.float16, (M, K), "X")
     _need(Y, torch.float16, (M, N), "Y")
     st = _lib.load().llmint8_matmul_noalloc(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW),
-                                            _ptr(Wq16), _ptr(W16), _ptr(Y), _stream(stream))
+                                            _ptr(Wq16), _ptr(W16), _ptr(Y), _stream(stream, X))
     _check(st, "llmint8_matmul_noalloc")
     return Y
 
 
 def llmint8_device_status(workspace, stream=None) -> int:
     """Synchronize and read (then clear) the device error word; returns a status code."""
-    return int(_lib.load().llmint8_device_status(_ptr(workspace), _stream(stream)))
+    return int(_lib.load().llmint8_device_status(_ptr(workspace), _stream(stream, workspace)))
 
 
 def llmint8_selftest_timeout(workspace, spin_limit: int, stream=None):
-    _check(_lib.load().llmint8_selftest_timeout(_ptr(workspace), int(spin_limit), _stream(stream)),
+    _check(_lib.load().llmint8_selftest_timeout(_ptr(workspace), int(spin_limit), _stream(stream, workspace)),
            "llmint8_selftest_timeout")
 
 
