@@ -290,6 +290,12 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
         return row_quant_vpt(K) == 1 ? launch_cluster(k_row_quant<1>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra)
                                      : launch_cluster(k_row_quant<2>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra);
     }
+    if (!L.decode && K <= 4096) {  // many short rows: one warp per row
+        const dim3 grid((M + kRowsPerCta - 1) / kRowsPerCta), block(kRowsPerCta * 32);
+        if (K <= 1024) return launch(k_row_quant_warp<4>, grid, block, 0, s, pdl, ra);
+        if (K <= 2048) return launch(k_row_quant_warp<8>, grid, block, 0, s, pdl, ra);
+        return launch(k_row_quant_warp<16>, grid, block, 0, s, pdl, ra);
+    }
     switch (row_quant_vpt(K)) {
         case 1: return launch(k_row_quant<1>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
         case 2: return launch(k_row_quant<2>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);

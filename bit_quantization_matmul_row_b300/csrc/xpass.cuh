@@ -365,6 +365,143 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
     if (row == 0 && tid == 0) a.hdr->outlier_count = n_out;
 }
 
+// A2 for many rows of at most 256 * VPL columns (prefill): one warp per row,
+// 8 rows per CTA.  The CTA reads the outlier bit map and forms its prefix once
+// for its 8 rows; each warp holds its row in registers (VPL 16-byte vectors
+// per lane), reduces the masked absmax with shuffles, writes the codes and
+// places its outlier values from the same registers.  No barrier sits between
+// the loads of a row and its codes, where the one-CTA-per-row kernel had four.
+constexpr int kRowsPerCta = 8;
+
+template <int VPL>
+__global__ void __launch_bounds__(kRowsPerCta * 32) k_row_quant_warp(RowQuantArgs a) {
+    constexpr int kWords = 8 * VPL;  // bit-map words of a row (<= the CTA's 256 threads)
+    static_assert(kWords <= kRowsPerCta * 32, "one bit-map word per thread");
+    __shared__ uint32_t s_bits[kWords];
+    __shared__ int32_t s_prefix[kWords];
+    __shared__ int32_t s_wsum[kRowsPerCta];
+    __shared__ int32_t s_total;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row = blockIdx.x * kRowsPerCta + warp;
+    const bool live = row < a.M;
+    const int K = a.K;
+    const int nwords = (K + 31) >> 5;
+    const int nvec = K >> 3;  // K % 16 == 0
+    pdl_trigger();
+    pdl_wait();
+
+    const __half* xrow = a.X + (size_t)(live ? row : 0) * K;
+    uint4 v[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int vi = lane + 32 * i;
+        v[i] = (live && vi < nvec) ? ldg_cg_v4(xrow + (size_t)vi * 8) : make_uint4(0, 0, 0, 0);
+    }
+    if (a.clear_status && blockIdx.x == 0 && tid == 0) a.hdr->status = 0u;
+
+    // --- bit map -> shared memory, exclusive prefix of popcounts (one word per thread) ---
+    const uint32_t b = (tid < nwords && !a.no_outliers) ? __ldcg(a.bitmap + tid) : 0u;
+    if (tid < kWords) s_bits[tid] = b;
+    const int cnt = __popc(b);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int w = 0; w < kRowsPerCta; ++w) {
+            const int y = s_wsum[w];
+            s_wsum[w] = run;
+            run += y;
+        }
+        s_total = run;
+    }
+    __syncthreads();
+    if (tid < kWords) s_prefix[tid] = s_wsum[warp] + incl - cnt;
+    __syncthreads();
+    const int n_out = s_total;
+
+    // --- masked absmax over the non-outlier columns of this row (warp) ---
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int c = 8 * (lane + 32 * i);
+        if (c < K) {
+            const uint32_t om = (s_bits[c >> 5] >> (c & 31)) & 0xFFu;
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                if (!((om >> (2 * e)) & 1u)) amax = fmaxf(amax, fabsf(f.x));
+                if (!((om >> (2 * e + 1)) & 1u)) amax = fmaxf(amax, fabsf(f.y));
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    // scale factor 127 / absmax in fp32, correctly rounded; absmax 0 -> 0
+    const float sf = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    if (!live) return;  // no barrier follows
+    if (lane == 0) a.row_scale[row] = amax;
+
+    // --- codes (outlier columns -> 0), outlier values and list from the registers ---
+    __half* xo_row = (a.xo != nullptr && n_out > 0) ? a.xo + (size_t)row * a.xo_pitch : nullptr;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int vi = lane + 32 * i, c = 8 * vi;
+        if (c >= K) continue;
+        const int wd = c >> 5, sh = c & 31;
+        const uint32_t word = s_bits[wd];
+        const uint32_t om = (word >> sh) & 0xFFu;
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        float q[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+            q[2 * e] = ((om >> (2 * e)) & 1u) ? 0.0f : code_of(f.x, sf);
+            q[2 * e + 1] = ((om >> (2 * e + 1)) & 1u) ? 0.0f : code_of(f.y, sf);
+        }
+        if (a.codes_fp16) {
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __half2 h = __floats2half2_rn(q[2 * e], q[2 * e + 1]);
+                o[e] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(static_cast<__half*>(a.codes) + (size_t)row * K + c) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            uint32_t o[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                o[e] = ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e]) | ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 1] << 8) |
+                       ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 2] << 16) |
+                       ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 3] << 24);
+            *reinterpret_cast<uint2*>(static_cast<int8_t*>(a.codes) + (size_t)row * K + c) = make_uint2(o[0], o[1]);
+        }
+        uint32_t bits = om;
+        while (bits) {
+            const int e = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int pos = s_prefix[wd] + __popc(word & ((1u << (sh + e)) - 1u));
+            if (xo_row) xo_row[pos] = __ushort_as_half((unsigned short)(w[e >> 1] >> (16 * (e & 1))));
+            if (row == 0) a.outlier_idx[pos] = c + e;
+        }
+    }
+    if (a.xo != nullptr) {
+        // zero padding up to the next multiple of 64 gathered columns
+        __half* xr = a.xo + (size_t)row * a.xo_pitch;
+        const int padded = (n_out + 63) & ~63;
+        for (int c = n_out + lane; c < padded; c += 32) xr[c] = __ushort_as_half(0);
+    }
+    if (row == 0 && lane == 0) a.hdr->outlier_count = n_out;
+}
+
 // A4 operand preparation for the tensor-core GEMM: W16oT[n, p] = W16[O[p], n]
 // for p < count, zero for count <= p < roundup(count, 64).  W16 is [K, N]
 // row-major; the result is [N, pitch] with the gathered K contiguous, the
