@@ -476,27 +476,35 @@ def run_prefill(args, dev, stream, bf16_peak, peak_src, iters=None):
         Y = torch.empty((c.M, c.N), dtype=torch.float16, device=dev)
         e0 = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
         e1 = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
-        e2 = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
 
-        def call(i, timed):
+        def call(i, timed):  # the public call, as a user runs it
             Wq_, sw_, Wq16_, Wd_ = reps[i % 2]
             if timed:
                 e0[i].record(stream)
-            api.llmint8_xpass(Xd, c.threshold, c.N, ws, stream=stream)
+            api.llmint8_matmul(Xd, c.threshold, Wq_, sw_, Wq16_, Wd_, Y=Y, workspace=ws, stream=stream)
             if timed:
                 e1[i].record(stream)
+
+        def split(i, timed):  # its two halves, with events around the GEMM stage
+            Wq_, sw_, Wq16_, Wd_ = reps[i % 2]
+            api.llmint8_xpass(Xd, c.threshold, c.N, ws, stream=stream)
+            if timed:
+                e0[i].record(stream)
             api.llmint8_gemm(Xd, c.threshold, Wq_, sw_, Wq16_, Wd_, Y, ws, stream=stream)
             if timed:
-                e2[i].record(stream)
+                e1[i].record(stream)
 
-        for i in range(3):
-            call(i, False)
-        torch.cuda.synchronize()
-        for i in range(iters):
-            call(i, True)
-        torch.cuda.synchronize()
-        call_ms = sum(e0[i].elapsed_time(e2[i]) for i in range(iters)) / iters
-        gemm_ms = sum(e1[i].elapsed_time(e2[i]) for i in range(iters)) / iters
+        def timed_ms(fn):
+            for i in range(3):
+                fn(i, False)
+            torch.cuda.synchronize()
+            for i in range(iters):
+                fn(i, True)
+            torch.cuda.synchronize()
+            return sum(e0[i].elapsed_time(e1[i]) for i in range(iters)) / iters
+
+        call_ms = timed_ms(call)
+        gemm_ms = timed_ms(split)
         flop = 2.0 * c.M * c.N * c.K
         n_o = api.read_intermediates(ws, c.M, c.K, c.N)["outlier_count"]
         out.append({"shape": [c.M, c.K, c.N], "outliers": n_o, "call_us": call_ms * 1e3, "gemm_us": gemm_ms * 1e3,

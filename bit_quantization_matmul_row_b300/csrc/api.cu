@@ -225,9 +225,17 @@ struct WsView {
     }
 };
 
-// A1 + A2 into the workspace.
+// Prefill rows of at most 4096 columns run k_row_quant_warp, which can also
+// write the gathered outlier rows of W16 for the GEMM (no separate gather).
+bool rowq_gathers_w16(bool decode, int K, float threshold, bool write_i32, const void* W16) {
+    const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
+    return !decode && K <= 4096 && use_outliers && !write_i32 && W16 != nullptr;
+}
+
+// A1 + A2 into the workspace; with gather_w16 also the A4 operand W16oT.
 llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* workspace, const Layout& L,
-                            DeviceInfo* dev, cudaStream_t s) {
+                            DeviceInfo* dev, cudaStream_t s, const void* W16 = nullptr, int N = 0,
+                            bool gather_w16 = false) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
     const WsView w(workspace, L);
     const __half* Xh = static_cast<const __half*>(X);
@@ -290,6 +298,10 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
         return row_quant_vpt(K) == 1 ? launch_cluster(k_row_quant<1>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra)
                                      : launch_cluster(k_row_quant<2>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra);
     }
+    ra.W16 = gather_w16 ? static_cast<const __half*>(W16) : nullptr;
+    ra.N = N;
+    ra.w16o = gather_w16 ? w.w16o : nullptr;
+    ra.w16o_pitch = L.kp;
     if (!L.decode && K <= 4096) {  // many short rows: one warp per row
         const dim3 grid((M + kRowsPerCta - 1) / kRowsPerCta), block(kRowsPerCta * 32);
         if (K <= 1024) return launch(k_row_quant_warp<4>, grid, block, 0, s, pdl, ra);
@@ -308,7 +320,8 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
 // A3 + A4 + A5 from the workspace an xpass_launch of the same problem filled.
 llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
                            const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
-                           void* workspace, const Layout& L, DeviceInfo* dev, cudaStream_t s) {
+                           void* workspace, const Layout& L, DeviceInfo* dev, cudaStream_t s,
+                           bool w16o_ready = false) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
     const WsView w(workspace, L);
     llmint8_status st;
@@ -354,8 +367,8 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
                          : launch(k_gemv_decode<2, false>, grid, block, gemv_dyn_smem(M), s, true, ga);
     }
 
-    // A4 operand: gathered, transposed outlier rows of W16
-    if (use_outliers && !write_i32) {
+    // A4 operand: gathered, transposed outlier rows of W16 (unless the X pass wrote it)
+    if (use_outliers && !write_i32 && !w16o_ready) {
         st = launch(k_gather_w16_outlier_rows, dim3((N + 63) / 64), dim3(256), 0, s, true,
                     static_cast<const __half*>(W16), N, (const WsHeader*)w.hdr, (const int32_t*)w.idx, w.w16o, L.kp);
         if (st != LLMINT8_OK) return st;
@@ -404,7 +417,8 @@ int kernels_per_call(int M, int K, int N, float threshold, bool write_i32) {
     // cluster: no scan kernel
     const bool scan = use_outliers && !cluster_flags_apply(M, K, threshold);
     int n = (scan ? 1 : 0) + 1 + 1;  // scan, row quant, GEMV / GEMM
-    if (M > LLMINT8_DECODE_MAX_M && use_outliers && !write_i32) n += 1;  // outlier rows of W16 for the GEMM
+    // outlier rows of W16 for the GEMM, unless the row quantization gathers them
+    if (M > LLMINT8_DECODE_MAX_M && use_outliers && !write_i32 && K > 4096) n += 1;
     (void)N;
     return n;
 }
@@ -419,8 +433,9 @@ llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, 
     if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, out, write_i32)) != LLMINT8_OK) return st;
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((st = xpass_launch(X, M, K, threshold, workspace, L, dev, s)) != LLMINT8_OK) return st;
-    return gemm_launch(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, out, write_i32, workspace, L, dev, s);
+    const bool gw = rowq_gathers_w16(L.decode, K, threshold, write_i32, W16);
+    if ((st = xpass_launch(X, M, K, threshold, workspace, L, dev, s, W16, N, gw)) != LLMINT8_OK) return st;
+    return gemm_launch(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, out, write_i32, workspace, L, dev, s, gw);
 }
 
 // Waits on a barrier nothing completes, bounded by spin_limit polls, then

@@ -116,6 +116,12 @@ struct RowQuantArgs {
     int no_outliers;          // threshold +inf: no scan ran, the bit map is not read
     int clear_status;         // no earlier kernel of this call reset the error word
     float t;                  // outlier threshold (cluster_flags)
+    // prefill only (k_row_quant_warp): also write the A4 operand of the GEMM,
+    // W16oT[n, p] = W16[O[p], n] (zero up to a multiple of 64); skipped if null
+    const __half* W16;        // [K, N]
+    int N;
+    __half* w16o;             // [N, w16o_pitch]
+    int w16o_pitch;
     int cluster_flags;        // launched as one cluster of M CTAs: the outlier columns are
                               // found here (no scan kernel, the bit map is not read)
 };
@@ -371,7 +377,13 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
 // per lane), reduces the masked absmax with shuffles, writes the codes and
 // places its outlier values from the same registers.  No barrier sits between
 // the loads of a row and its codes, where the one-CTA-per-row kernel had four.
+//
+// With w16o set, the CTAs also write the A4 operand of the tensor-core GEMM,
+// W16oT[n, p] = W16[O[p], n] (zero for count <= p < a multiple of 64), each CTA
+// a share of the 16-column groups of N, through a shared-memory transpose: the
+// outlier list is already here, so no separate gather launch is needed.
 constexpr int kRowsPerCta = 8;
+constexpr int kGatherCols = 16;
 
 template <int VPL>
 __global__ void __launch_bounds__(kRowsPerCta * 32) k_row_quant_warp(RowQuantArgs a) {
@@ -381,6 +393,8 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) k_row_quant_warp(RowQuantArg
     __shared__ int32_t s_prefix[kWords];
     __shared__ int32_t s_wsum[kRowsPerCta];
     __shared__ int32_t s_total;
+    __shared__ int32_t s_idx[32 * kWords];                    // the outlier list, for the gather
+    __shared__ __align__(16) __half s_tile[64][kGatherCols];  // 64 outliers x 16 columns
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x * kRowsPerCta + warp;
@@ -422,84 +436,131 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) k_row_quant_warp(RowQuantArg
         s_total = run;
     }
     __syncthreads();
-    if (tid < kWords) s_prefix[tid] = s_wsum[warp] + incl - cnt;
+    const bool gather = a.w16o != nullptr;
+    if (tid < kWords) {
+        const int pre = s_wsum[warp] + incl - cnt;
+        s_prefix[tid] = pre;
+        if (gather) {  // positions of this word's outliers in the list
+            uint32_t bb = b;
+            for (int k = pre; bb; ++k) {
+                s_idx[k] = 32 * tid + __ffs(bb) - 1;
+                bb &= bb - 1;
+            }
+        }
+    }
     __syncthreads();
     const int n_out = s_total;
 
-    // --- masked absmax over the non-outlier columns of this row (warp) ---
-    float amax = 0.0f;
+    // --- this warp's row ---
+    if (live) {
+        // masked absmax over the non-outlier columns
+        float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int c = 8 * (lane + 32 * i);
-        if (c < K) {
-            const uint32_t om = (s_bits[c >> 5] >> (c & 31)) & 0xFFu;
+        for (int i = 0; i < VPL; ++i) {
+            const int c = 8 * (lane + 32 * i);
+            if (c < K) {
+                const uint32_t om = (s_bits[c >> 5] >> (c & 31)) & 0xFFu;
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                    if (!((om >> (2 * e)) & 1u)) amax = fmaxf(amax, fabsf(f.x));
+                    if (!((om >> (2 * e + 1)) & 1u)) amax = fmaxf(amax, fabsf(f.y));
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        // scale factor 127 / absmax in fp32, correctly rounded; absmax 0 -> 0
+        const float sf = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+        if (lane == 0) a.row_scale[row] = amax;
+
+        // codes (outlier columns -> 0), outlier values and list from the registers
+        __half* xo_row = (a.xo != nullptr && n_out > 0) ? a.xo + (size_t)row * a.xo_pitch : nullptr;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int vi = lane + 32 * i, c = 8 * vi;
+            if (c >= K) continue;
+            const int wd = c >> 5, sh = c & 31;
+            const uint32_t word = s_bits[wd];
+            const uint32_t om = (word >> sh) & 0xFFu;
             const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            float q[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-                if (!((om >> (2 * e)) & 1u)) amax = fmaxf(amax, fabsf(f.x));
-                if (!((om >> (2 * e + 1)) & 1u)) amax = fmaxf(amax, fabsf(f.y));
+                q[2 * e] = ((om >> (2 * e)) & 1u) ? 0.0f : code_of(f.x, sf);
+                q[2 * e + 1] = ((om >> (2 * e + 1)) & 1u) ? 0.0f : code_of(f.y, sf);
+            }
+            if (a.codes_fp16) {
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    __half2 h = __floats2half2_rn(q[2 * e], q[2 * e + 1]);
+                    o[e] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                *reinterpret_cast<uint4*>(static_cast<__half*>(a.codes) + (size_t)row * K + c) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            } else {
+                uint32_t o[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    o[e] = ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e]) |
+                           ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 1] << 8) |
+                           ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 2] << 16) |
+                           ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 3] << 24);
+                *reinterpret_cast<uint2*>(static_cast<int8_t*>(a.codes) + (size_t)row * K + c) =
+                    make_uint2(o[0], o[1]);
+            }
+            uint32_t bits = om;
+            while (bits) {
+                const int e = __ffs(bits) - 1;
+                bits &= bits - 1;
+                const int pos = s_prefix[wd] + __popc(word & ((1u << (sh + e)) - 1u));
+                if (xo_row) {
+                    const uint32_t w32 = (e & 4) ? ((e & 2) ? w[3] : w[2]) : ((e & 2) ? w[1] : w[0]);
+                    xo_row[pos] = __ushort_as_half((unsigned short)(w32 >> (16 * (e & 1))));
+                }
+                if (row == 0) a.outlier_idx[pos] = c + e;
             }
         }
+        if (a.xo != nullptr) {
+            // zero padding up to the next multiple of 64 gathered columns
+            __half* xr = a.xo + (size_t)row * a.xo_pitch;
+            const int padded = (n_out + 63) & ~63;
+            for (int c = n_out + lane; c < padded; c += 32) xr[c] = __ushort_as_half(0);
+        }
+        if (row == 0 && lane == 0) a.hdr->outlier_count = n_out;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    // scale factor 127 / absmax in fp32, correctly rounded; absmax 0 -> 0
-    const float sf = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-    if (!live) return;  // no barrier follows
-    if (lane == 0) a.row_scale[row] = amax;
 
-    // --- codes (outlier columns -> 0), outlier values and list from the registers ---
-    __half* xo_row = (a.xo != nullptr && n_out > 0) ? a.xo + (size_t)row * a.xo_pitch : nullptr;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int vi = lane + 32 * i, c = 8 * vi;
-        if (c >= K) continue;
-        const int wd = c >> 5, sh = c & 31;
-        const uint32_t word = s_bits[wd];
-        const uint32_t om = (word >> sh) & 0xFFu;
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        float q[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-            q[2 * e] = ((om >> (2 * e)) & 1u) ? 0.0f : code_of(f.x, sf);
-            q[2 * e + 1] = ((om >> (2 * e + 1)) & 1u) ? 0.0f : code_of(f.y, sf);
-        }
-        if (a.codes_fp16) {
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                __half2 h = __floats2half2_rn(q[2 * e], q[2 * e + 1]);
-                o[e] = *reinterpret_cast<uint32_t*>(&h);
-            }
-            *reinterpret_cast<uint4*>(static_cast<__half*>(a.codes) + (size_t)row * K + c) =
-                make_uint4(o[0], o[1], o[2], o[3]);
-        } else {
-            uint32_t o[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-                o[e] = ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e]) | ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 1] << 8) |
-                       ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 2] << 16) |
-                       ((uint32_t)(uint8_t)(int8_t)(int)q[4 * e + 3] << 24);
-            *reinterpret_cast<uint2*>(static_cast<int8_t*>(a.codes) + (size_t)row * K + c) = make_uint2(o[0], o[1]);
-        }
-        uint32_t bits = om;
-        while (bits) {
-            const int e = __ffs(bits) - 1;
-            bits &= bits - 1;
-            const int pos = s_prefix[wd] + __popc(word & ((1u << (sh + e)) - 1u));
-            if (xo_row) xo_row[pos] = __ushort_as_half((unsigned short)(w[e >> 1] >> (16 * (e & 1))));
-            if (row == 0) a.outlier_idx[pos] = c + e;
-        }
-    }
-    if (a.xo != nullptr) {
-        // zero padding up to the next multiple of 64 gathered columns
-        __half* xr = a.xo + (size_t)row * a.xo_pitch;
+    // --- A4 operand of the GEMM: W16oT for this CTA's 16-column groups ---
+    if (gather && n_out > 0) {
         const int padded = (n_out + 63) & ~63;
-        for (int c = n_out + lane; c < padded; c += 32) xr[c] = __ushort_as_half(0);
+        const int groups = a.N / kGatherCols;
+        for (int gp = blockIdx.x; gp < groups; gp += gridDim.x) {
+            const int n0 = gp * kGatherCols;
+            for (int p0 = 0; p0 < padded; p0 += 64) {
+                {   // read: outlier p0 + p, columns n0 + 4j .. +3 (8 bytes of one W16 row)
+                    const int p = tid >> 2, j = (tid & 3) * 4;
+                    uint2 val = make_uint2(0u, 0u);
+                    if (p0 + p < n_out)
+                        val = *reinterpret_cast<const uint2*>(a.W16 + (size_t)s_idx[p0 + p] * a.N + n0 + j);
+                    *reinterpret_cast<uint2*>(&s_tile[p][j]) = val;
+                }
+                __syncthreads();
+                {   // write: row n0 + jn of W16oT, outliers p0 + 4q .. +3
+                    const int jn = tid >> 4, q4 = (tid & 15) * 4;
+                    const uint32_t lo = (uint32_t)__half_as_ushort(s_tile[q4][jn]) |
+                                        ((uint32_t)__half_as_ushort(s_tile[q4 + 1][jn]) << 16);
+                    const uint32_t hi = (uint32_t)__half_as_ushort(s_tile[q4 + 2][jn]) |
+                                        ((uint32_t)__half_as_ushort(s_tile[q4 + 3][jn]) << 16);
+                    *reinterpret_cast<uint2*>(a.w16o + (size_t)(n0 + jn) * a.w16o_pitch + p0 + q4) =
+                        make_uint2(lo, hi);
+                }
+                __syncthreads();
+            }
+        }
     }
-    if (row == 0 && lane == 0) a.hdr->outlier_count = n_out;
 }
 
 // A4 operand preparation for the tensor-core GEMM: W16oT[n, p] = W16[O[p], n]

@@ -135,8 +135,10 @@ def test_kernels_per_call(lib):
     for M, K in ((1, 4112), (1, 16384), (16, 11008), (16, 65536)):
         assert k(M, K, 4096, 6.0, 0) == 3, (M, K)
         assert k(M, K, 4096, inf, 0) == 2       # no outlier scan
-    # prefill: scan + row quantization + outlier rows of W16 + GEMM
-    assert k(17, 4096, 4096, 6.0, 0) == 4
+    # prefill: scan + row quantization (which also gathers the outlier rows of W16
+    # when rows have at most 4096 columns) + GEMM
+    assert k(17, 4096, 4096, 6.0, 0) == 3
+    assert k(17, 4112, 4096, 6.0, 0) == 4       # separate gather of the outlier rows of W16
     assert k(17, 4096, 4096, 6.0, 1) == 3       # the int32 result leaves out the fp16 slice
     assert k(17, 4096, 4096, inf, 0) == 2
     assert k(0, 64, 64, 6.0, 0) == -1
