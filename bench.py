@@ -525,6 +525,60 @@ def run_prefill(args, dev, stream, bf16_peak, peak_src, iters=None):
             "shapes": out}
 
 
+def run_ablation(args):
+    """Error vs speed of the LLM.int8() decomposition against plain vector-wise int8
+    (threshold +inf: no outlier decomposition) and the fp16 matmul (cuBLAS, context),
+    on the synthetic outlier workloads.  Error: relative Frobenius distance to the
+    exact product (fp64 on the GPU).  Times: CUDA events around single calls."""
+    import torch
+    from bit_quantization_matmul_row_b300 import api
+    dev = torch.device("cuda")
+    torch.cuda.set_device(0)
+    cases = [("decode 7B M=1 4096x4096 0.1%", 1, 4096, 4096, 0.001),
+             ("decode 7B M=16 4096x11008 0.1%", 16, 4096, 11008, 0.001),
+             ("prefill 7B M=2048 4096x4096 0.1%", 2048, 4096, 4096, 0.001)]
+    for f in (0.0, 0.001, 0.01, 0.05):
+        cases.append((f"70B M=256 8192x8192 {100 * f:g}%", 256, 8192, 8192, f))
+    R = 4  # rotating weight replicas: every timed call streams its weights from HBM
+    rows = []
+    for name, M, K, N, frac in cases:
+        X, _ = synthetic.make_x(M, K, frac=frac, min_count=4 if frac > 0 else 0, seed=M + K + N)
+        W, _ = synthetic.make_w(K, N, sigma=0.015 if K == 8192 else 0.02, seed=M + K + N)
+        Xd, Wd = torch.from_numpy(X).to(dev), torch.from_numpy(W).to(dev)
+        Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd, fp16_codes=M > 16)
+        reps = [(Wq, sw, Wq16, Wd)] + [(Wq.clone(), sw.clone(), None if Wq16 is None else Wq16.clone(), Wd.clone())
+                                       for _ in range(R - 1)]
+        ws = api.make_workspace(M, K, N, dev)
+        exact = Xd.double() @ Wd.double()
+        variants = {
+            "llmint8_t6": lambda r: api.llmint8_matmul(Xd, 6.0, r[0], r[1], r[2], r[3], workspace=ws),
+            "int8_no_outliers": lambda r: api.llmint8_matmul_int8(Xd, r[0], r[1], r[2], workspace=ws),
+            "fp16_cublas": lambda r: torch.matmul(Xd, r[3]),
+        }
+        row = {"case": name, "M": M, "K": K, "N": N, "outlier_frac": frac}
+        for key, fn in variants.items():
+            Y = fn(reps[0])
+            torch.cuda.synchronize()
+            err = float(torch.linalg.norm(Y.double() - exact) / torch.linalg.norm(exact))
+            if key == "llmint8_t6":
+                row["n_outliers"] = api.read_intermediates(ws, M, K, N)["outlier_count"]
+            for i in range(5):
+                fn(reps[i % R])
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(20):
+                fn(reps[i % R])
+            e1.record()
+            torch.cuda.synchronize()
+            row[key] = {"rel_error": err, "us": 1e3 * e0.elapsed_time(e1) / 20}
+        rows.append(row)
+        del Xd, Wd, Wq, sw, Wq16, reps, ws, exact
+        torch.cuda.empty_cache()
+    print(json.dumps({"ablation": rows, "data": "synthetic", "note": (
+        "per-tensor scales change only the scale arrays, not the kernels' work, so their speed is the "
+        "vector-wise path's; their error is measured with the CPU oracle in the tests")}), flush=True)
+
+
 def run_profile(args):
     """Eager calls of one named case (warmup + steps), for profiler captures."""
     import torch
@@ -567,6 +621,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--max-graphs", type=int, default=256)
+    ap.add_argument("--ablation", action="store_true",
+                    help="error vs speed: LLM.int8() against plain int8 and the fp16 matmul (one JSON line)")
     ap.add_argument("--profile", metavar="CASE", default=None,
                     help="run only the named synthetic case (eager calls; for ncu captures)")
     args = ap.parse_args()
@@ -575,6 +631,9 @@ def main():
     world, rank, local = dist_setup()
     if args.profile:
         run_profile(args)
+        return
+    if args.ablation:
+        run_ablation(args)
         return
     if args.impl == "reference":
         run_reference(args, world, rank)

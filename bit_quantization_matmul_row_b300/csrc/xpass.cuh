@@ -69,13 +69,15 @@ __global__ void __launch_bounds__(kScanThreads) k_outlier_scan(const __half* __r
         const __half* p = X + c0;
         int r = blockIdx.y * 8 + warp;
         const int step = gridDim.y * 8;
-        // two independent loads in flight per iteration
-        for (; r + step < M; r += 2 * step) {
-            const uint4 a = ldg_cg_v4(p + (size_t)r * K);
-            const uint4 b = ldg_cg_v4(p + (size_t)(r + step) * K);
-            m |= outlier_mask8(a, t) | outlier_mask8(b, t);
+        // four independent loads in flight per iteration (a warp walks ~M / (8 gy) rows)
+        for (; r + 3 * step < M; r += 4 * step) {
+            uint4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = ldg_cg_v4(p + (size_t)(r + u * step) * K);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) m |= outlier_mask8(x[u], t);
         }
-        if (r < M) m |= outlier_mask8(ldg_cg_v4(p + (size_t)r * K), t);
+        for (; r < M; r += step) m |= outlier_mask8(ldg_cg_v4(p + (size_t)r * K), t);
     }
     // lanes 4w..4w+3 hold the 32 columns of bitmap word w of this strip
     uint32_t word = m << (8 * (lane & 3));

@@ -62,11 +62,13 @@ def _load():
             lib.oracle_code.restype = ctypes.c_int8
             lib.oracle_quantize_weight.argtypes = [P, I, I, P, P]
             lib.oracle_outlier_columns.argtypes = [P, I, I, ctypes.c_float, P]
+            lib.oracle_quantize_per_tensor.argtypes = [P, I, P, P]
             lib.oracle_quantize_rows.argtypes = [P, I, I, P, P, P]
             lib.oracle_int8_matmul.argtypes = [P, P, I, I, I, P, ctypes.c_int]
             lib.oracle_outlier_matmul.argtypes = [P, P, P, I, I, I, P, ctypes.c_int]
             lib.oracle_merge.argtypes = [P, P, P, P, I, I, P]
             for f in ("oracle_quantize_weight", "oracle_outlier_columns", "oracle_quantize_rows",
+                      "oracle_quantize_per_tensor",
                       "oracle_int8_matmul", "oracle_outlier_matmul", "oracle_merge"):
                 getattr(lib, f).restype = None
             _lib = lib
@@ -188,6 +190,24 @@ def merge(C: np.ndarray, s_x: np.ndarray, s_w: np.ndarray, F: np.ndarray | None)
     Y = np.empty((M, N), np.uint16)
     _load().oracle_merge(_ptr(C), _ptr(sx), _ptr(sw), Fp, M, N, _ptr(Y))
     return Y.view(np.float16)
+
+
+def quantize_per_tensor(A: np.ndarray):
+    """Ablation: one scale for the whole fp16 tensor -> (codes int8, same shape; absmax float32)."""
+    Ab = np.ascontiguousarray(_bits(A))
+    q = np.empty(Ab.shape, np.int8)
+    s = np.empty(1, np.float32)
+    _load().oracle_quantize_per_tensor(_ptr(Ab), Ab.size, _ptr(q), _ptr(s))
+    return q, s[0]
+
+
+def per_tensor_int8_matmul(X: np.ndarray, W: np.ndarray, nthreads: int | None = None) -> np.ndarray:
+    """Ablation: Y = X.W with one scale per tensor for X and W, no outlier decomposition."""
+    Xq, sx = quantize_per_tensor(X)
+    Wq, sw = quantize_per_tensor(W)
+    C = int8_matmul(Xq, Wq, nthreads)
+    M, N = C.shape
+    return merge(C, np.full(M, sx, np.float32), np.full(N, sw, np.float32), None)
 
 
 def outlier_indices(is_outlier: np.ndarray) -> np.ndarray:

@@ -131,6 +131,25 @@ void oracle_quantize_weight(const uint16_t *W, int64_t K, int64_t N, int8_t *Wq,
 }
 
 /* ---------------------------------------------------------------------------
+ * Ablation, not a step of the path: per-tensor quantization, the coarse
+ * granularity [FABRIC] section 3.4 contrasts with per-channel scales.  One
+ * absmax over all n values of a tensor, then the same code rule as A0/A2.
+ * ------------------------------------------------------------------------- */
+void oracle_quantize_per_tensor(const uint16_t *A, int64_t n, int8_t *q, float *s)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(half_to_float(A[i]));
+        if (a > amax)
+            amax = a;
+    }
+    *s = amax;
+    float sf = oracle_scale_factor(amax);
+    for (int64_t i = 0; i < n; ++i)
+        q[i] = oracle_code(half_to_float(A[i]), sf);
+}
+
+/* ---------------------------------------------------------------------------
  * A1. Outlier dimensions ([WALK] section 2.3): a K-column of X whose largest
  * magnitude exceeds the threshold t (default 6.0) is an outlier column.
  * "Exceeds" is read as strict: |x| > t.

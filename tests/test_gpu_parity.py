@@ -248,3 +248,16 @@ SWEEP = [c for c in synthetic.sweep_70b()
 @pytest.mark.parametrize("case", SWEEP, ids=lambda c: c.name)
 def test_sweep_70b(case):
     _full_case(case, nrows=12)
+
+
+@pytest.mark.parametrize("M,K,N", [(4, 4096, 512), (512, 2048, 512)])
+def test_decomposition_beats_plain_int8_on_outlier_inputs(M, K, N):
+    # With outlier columns present, the LLM.int8() result (threshold 6) is several
+    # times closer to the exact product than plain vector-wise int8 (threshold
+    # +inf) computed by the same kernels: the claim the pages make for the method.
+    X, W = xw(M, K, N, frac=0.01, seed=M + 900, min_count=4)
+    exact = X.astype(np.float64) @ W.astype(np.float64)
+    g6 = run_gpu(X, W, 6.0, want_i32=False)
+    gi = run_gpu(X, W, math.inf, want_i32=False)
+    err = lambda Y: np.linalg.norm(Y.astype(np.float64) - exact) / np.linalg.norm(exact)
+    assert err(g6["Y"]) * 4 < err(gi["Y"])

@@ -306,3 +306,45 @@ def test_row_subset_matches_full(oracle_mod):
     sub = oracle_mod.llmint8_matmul(X, W, 6.0, rows=rows)
     assert np.array_equal(sub["Y"].view(np.uint16), full["Y"][rows].view(np.uint16))
     assert np.array_equal(sub["C"], full["C"][rows])
+
+
+# ---------------------------------------------------------------------------
+# Ablation (not a step of the path): per-tensor scales and plain int8 without the
+# outlier decomposition, the schemes the pages contrast LLM.int8() with.
+
+def test_per_tensor_codes_closed_form(oracle_mod):
+    # one scale for the whole tensor: absmax 4 -> factor 127/4 = 31.75;
+    # 2 -> 63.5 -> 64 (tie away from zero), -1 -> -31.75 -> -32, 0.5 -> 15.875 -> 16
+    X = np.array([[2.0, -1.0], [0.5, 4.0]], np.float16)
+    q, s = oracle_mod.quantize_per_tensor(X)
+    assert s == np.float32(4.0)
+    assert q.tolist() == [[64, -32], [16, 127]]
+
+
+@pytest.mark.parametrize("M,K,N,frac,seed", [(64, 1024, 256, 0.01, 1), (16, 4096, 256, 0.001, 2),
+                                             (128, 2048, 256, 0.05, 3)])
+def test_outliers_break_plain_int8_but_not_the_decomposition(oracle_mod, M, K, N, frac, seed):
+    # The pitfalls guide's table and the paper walkthrough: without outlier handling
+    # int8 loses much more accuracy than LLM.int8(); coarser (per-tensor) scales
+    # lose more still.  Relative Frobenius error against the exact product.
+    X, _ = synthetic.make_x(M, K, frac=frac, min_count=4, seed=seed)
+    W, _ = synthetic.make_w(K, N, seed=seed)
+    exact = X.astype(np.float64) @ W.astype(np.float64)
+    err = lambda Y: np.linalg.norm(Y.astype(np.float64) - exact) / np.linalg.norm(exact)
+    e_llm = err(oracle_mod.llmint8_matmul(X, W, 6.0)["Y"])
+    e_naive = err(oracle_mod.llmint8_matmul(X, W, math.inf)["Y"])
+    e_tensor = err(oracle_mod.per_tensor_int8_matmul(X, W))
+    assert e_llm * 4 < e_naive < e_tensor
+    assert e_llm < 0.02
+
+
+def test_without_outliers_the_decomposition_is_plain_int8(oracle_mod):
+    X, _ = synthetic.make_x(32, 1024, frac=0.0, seed=4)
+    W, _ = synthetic.make_w(1024, 512, seed=4)
+    assert not oracle_mod.outlier_columns(X, 6.0).any()
+    y_llm = oracle_mod.llmint8_matmul(X, W, 6.0)["Y"]
+    y_naive = oracle_mod.llmint8_matmul(X, W, math.inf)["Y"]
+    assert np.array_equal(y_llm.view(np.uint16), y_naive.view(np.uint16))
+    exact = X.astype(np.float64) @ W.astype(np.float64)
+    err = lambda Y: np.linalg.norm(Y.astype(np.float64) - exact) / np.linalg.norm(exact)
+    assert err(y_naive) <= err(oracle_mod.per_tensor_int8_matmul(X, W))
