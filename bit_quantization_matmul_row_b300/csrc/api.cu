@@ -265,7 +265,7 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
     }
 
     // A2: row scales and codes (+ the gathered outlier columns of X)
-    RowQuantArgs ra;
+    RowQuantArgs ra{};
     ra.X = Xh;
     ra.M = M;
     ra.K = K;
@@ -347,22 +347,38 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         {
             std::lock_guard<std::mutex> lock(g_mu);
             if (!dev->gemv_attr_set) {
-                if (cudaFuncSetAttribute(k_gemv_decode<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemv_dyn_smem(8)) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemv_dyn_smem(8)) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemv_dyn_smem(16)) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemv_dyn_smem(16)) != cudaSuccess)
+                const int m8 = (int)gemv_dyn_smem(8), m16 = (int)gemv_dyn_smem(16);
+                if (cudaFuncSetAttribute(k_gemv_decode<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         m8) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         m8) != cudaSuccess)
                     return LLMINT8_ECUDA;
                 dev->gemv_attr_set = true;
             }
         }
-        const dim3 grid(N / kGemvCols), block(kGemvWarps * 32);
-        if (M <= 8)
+        const dim3 block(kGemvWarps * 32);
+        const int ntiles = N / kGemvCols, slots = 2 * dev->sms;  // two CTAs per SM
+        if (M <= 8) {
+            if (ntiles > slots) {  // one-tile CTAs would need several waves: persistent grid
+                const dim3 grid(slots);
+                return write_i32 ? launch(k_gemv_decode_tiles<1, true>, grid, block, gemv_dyn_smem(M), s, true, ga)
+                                 : launch(k_gemv_decode_tiles<1, false>, grid, block, gemv_dyn_smem(M), s, true, ga);
+            }
+            const dim3 grid(ntiles);
             return write_i32 ? launch(k_gemv_decode<1, true>, grid, block, gemv_dyn_smem(M), s, true, ga)
                              : launch(k_gemv_decode<1, false>, grid, block, gemv_dyn_smem(M), s, true, ga);
+        }
+        // up to 16 rows: the persistent form measured slower (its per-tile
+        // epilogue costs more than the waves it removes), one-tile CTAs
+        const dim3 grid(ntiles);
         return write_i32 ? launch(k_gemv_decode<2, true>, grid, block, gemv_dyn_smem(M), s, true, ga)
                          : launch(k_gemv_decode<2, false>, grid, block, gemv_dyn_smem(M), s, true, ga);
     }

@@ -99,6 +99,22 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
 
+// Hint: bring [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
+// It moves nothing into the SM, so it may precede griddepcontrol.wait even for
+// data the predecessor writes: every read after the wait goes through L2, which
+// also receives those writes.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 32-bit load through L2, kept in program order (issued where it is written, so
+// independent loads go out together).
+__device__ __forceinline__ int ldg_cg_s32(const int* p) {
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }

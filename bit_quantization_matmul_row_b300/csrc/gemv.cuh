@@ -151,14 +151,18 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
     const float rs = (!WRITE_I32 && active) ? __ldcg(a.row_scale + ri) : 0.0f;
 
     // A4 operands of this CTA's 16 columns for outlier positions [base, base + c):
-    // the W16 rows (32 bytes each) and the gathered X values.  The index loads do
-    // not wait for the count: positions past it are loaded but not used.
-    const int cnt = (!WRITE_I32 && a.use_outliers) ? __ldcg(&a.hdr->outlier_count) : 0;
+    // the W16 rows (32 bytes each) and the gathered X values.  The indices of the
+    // first chunk are requested together with the count (positions past it are
+    // loaded but not used), so the W16 gather waits for one L2 round trip.
+    static_assert(2 * kGemvOutChunk <= kGemvWarps * 32, "one (outlier, half-row) per thread");
+    const bool outl = !WRITE_I32 && a.use_outliers;
     const int nidx = min(K, kGemvOutChunk);
+    const int k_first = (outl && (tid >> 1) < nidx) ? ldg_cg_s32(a.outlier_idx + (tid >> 1)) : 0;
+    const int cnt = outl ? ldg_cg_s32(&a.hdr->outlier_count) : 0;
     auto stage_outliers = [&](int base, int c) {
         for (int e = tid; e < 2 * nidx; e += kGemvWarps * 32) {
             const int j = e >> 1, hv = e & 1;
-            const int k = base + j < K ? __ldcg(a.outlier_idx + base + j) : 0;
+            const int k = base == 0 ? k_first : (base + j < K ? __ldcg(a.outlier_idx + base + j) : 0);
             if (j < c) cp_async16(&s_w16o[j][hv * 8], a.W16 + (size_t)k * a.N + n0 + hv * 8);
         }
         const int cv = (c + 7) >> 3;
@@ -178,26 +182,50 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
     for (int t = 0; t < MT; ++t)
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[t][r] = 0;
+    // Main loop, unrolled by the ring depth: ring offsets and the offsets of the
+    // refill sources are constants, the sources advance by R steps per round.
+    // Steps [0, nfull) are whole 64-byte steps inside the warp's K slice; only a
+    // ragged last step (K not a multiple of 64) takes the checked path.
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int s = 0; s < nsteps; ++s) {
-        if (s == 0)
-            cp_async_wait_group<1>();      // the first R steps, both halves (staging may be pending)
-        else if (s >= R)
-            cp_async_wait_group<R - 1>();  // the refill of step s was committed R - 1 groups ago
-        const uint8_t* slot = slot_of(s);
-        const uint4 w0 = *reinterpret_cast<const uint4*>(slot);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(slot + 512);
-        const bool ok = step_ok(s);
+    const int nfull = kend > kb0 ? (kend - kb0) >> 6 : 0;
+    uint8_t* const my_ring = ring + lane * 16;
+    const int8_t* wr = w0p + R * 64;  // refill source of step R: row n0+g; row n0+g+8 is 8K further
+    const int8_t* xr[MT];
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
-            const uint4 xf = (ok && xok[t]) ? *reinterpret_cast<const uint4*>(slot + 1024 + 512 * t) : z;
-            imma_16832(acc[t], w0.x, w1.x, w0.y, w1.y, xf.x, xf.y);
-            imma_16832(acc[t], w0.z, w1.z, w0.w, w1.w, xf.z, xf.w);
+    for (int t = 0; t < MT; ++t) xr[t] = xp[t] + R * 64;
+    for (int base = 0; base < nsteps; base += R) {
+#pragma unroll
+        for (int d = 0; d < R; ++d) {
+            const int s = base + d;
+            if (s >= nsteps) break;
+            if (base > 0)
+                cp_async_wait_group<R - 1>();  // the refill of step s was committed R - 1 groups ago
+            else if (d == 0)
+                cp_async_wait_group<1>();      // the first R steps, both halves (staging may be pending)
+            uint8_t* slot = my_ring + d * SLOT;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(slot);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(slot + 512);
+            const bool ok = s < nfull || kb0 + s * 64 + 16 * tq < kend;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                const uint4 xf = (ok && xok[t]) ? *reinterpret_cast<const uint4*>(slot + 1024 + 512 * t) : z;
+                imma_16832(acc[t], w0.x, w1.x, w0.y, w1.y, xf.x, xf.y);
+                imma_16832(acc[t], w0.z, w1.z, w0.w, w1.w, xf.z, xf.w);
+            }
+            // the slot's values were consumed by the MMAs above: refill it with step s + R
+            const int sr = s + R;
+            if (sr < nfull || (sr < nsteps && kb0 + sr * 64 + 16 * tq < kend)) {
+                cp_async16(slot, wr + d * 64);
+                cp_async16(slot + 512, wr + (size_t)8 * K + d * 64);
+#pragma unroll
+                for (int t = 0; t < MT; ++t)
+                    if (xok[t]) cp_async16(slot + 1024 + 512 * t, xr[t] + d * 64);
+            }
+            cp_async_commit();
         }
-        // the slot's values were consumed by the MMAs above: refill it
-        issue_w(s + R);
-        issue_x(s + R);
-        cp_async_commit();
+        wr += R * 64;
+#pragma unroll
+        for (int t = 0; t < MT; ++t) xr[t] += R * 64;
     }
 
     // No copy may still target shared memory: the ring is drained (its later
@@ -244,6 +272,222 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
         const float scale = rs * cs * (1.0f / 16129.0f);
         reinterpret_cast<__half*>(a.out)[(size_t)ri * a.N + n] = __float2half_rn(fmaf((float)c, scale, f));
     }
+}
+
+// Persistent form for shapes with more 16-column tiles than resident CTAs
+// (two per SM), used for up to 8 rows of X.  One-tile CTAs would run in several waves, and every later
+// wave would start its weight stream from an empty ring while the SM's share
+// of HBM idles.  Here the grid is exactly the resident CTAs; CTA b takes tiles
+// b, b + G, b + 2G, ... (G = grid size), and each warp's ring runs on across
+// the CTA's tiles, so the next tile's weights stream while the current one is
+// reduced and written.  The first ring steps are requested before the
+// dependency wait, as in the one-tile kernel.
+//
+// Tile epilogue, between two CTA barriers: the 8 warps' partials are summed in
+// shared memory, the fp16 outlier slice (A4) is added from staged operands and
+// the scale outer product applied (A5).  The gathered X values of the first
+// kTileOutChunk outliers are staged once; the matching W16 rows of the next
+// tile are staged during the current one (double-buffered).  Outliers past the
+// chunk are read through L2 in the epilogue.
+//
+// Commit groups of every thread, in order: one per weight step before the wait
+// (R), the X halves of those steps, the staging of tile 0 (X values and W16
+// rows), then one per refilled step, and after each tile but the last the W16
+// staging of the next tile.
+constexpr int kTileOutChunk = 64;
+
+template <int MT, bool WRITE_I32>
+__global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode_tiles(GemvArgs a) {
+    constexpr int R = gemv_ring(MT);
+    constexpr int MR = 8 * MT;  // rows of X held by the fragments
+    const int SLOT = gemv_slot(a.M);
+    __shared__ int32_t s_red[kGemvWarps][MR][kGemvCols];                   // int8 partials of one tile
+    __shared__ __align__(16) __half s_w16o[2][kTileOutChunk][kGemvCols];  // W16[O[j], tile columns]
+    __shared__ __align__(16) __half s_xo[MR][kTileOutChunk];              // X[i, O[j]]
+    __shared__ int32_t s_idx[kTileOutChunk];                               // O[j]
+    extern __shared__ __align__(16) uint8_t s_ring_all[];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tq = lane & 3;
+    const int K = a.K;
+    const int kb0 = warp * a.k_per_warp;
+    const int kend = min(K, kb0 + a.k_per_warp);
+    const int nsteps = kend > kb0 ? (kend - kb0 + 63) >> 6 : 0;
+    const int G = gridDim.x;
+    const int my_tiles = (a.N / kGemvCols - (int)blockIdx.x + G - 1) / G;  // >= 1: the grid has <= tiles CTAs
+    const int total = my_tiles * nsteps;
+    auto tile_n0 = [&](int j) { return ((int)blockIdx.x + j * G) * kGemvCols; };
+
+    const int8_t* xp[MT];
+    bool xok[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        const int i = g + 8 * t;
+        xok[t] = i < a.M;
+        xp[t] = a.codes + (size_t)(xok[t] ? i : 0) * K + kb0 + 16 * tq;
+    }
+    uint8_t* ring = s_ring_all + (size_t)warp * R * SLOT;
+    auto slot_of = [&](int u) { return ring + (u % R) * SLOT + lane * 16; };
+    auto step_ok = [&](int st) { return st < nsteps && kb0 + st * 64 + 16 * tq < kend; };
+    // flattened step u = (tile j of this CTA) * nsteps + (step st of the warp's K slice)
+    auto issue_w = [&](int u) {
+        if (u < total) {
+            const int j = u / nsteps, st = u - j * nsteps;
+            if (step_ok(st)) {
+                const int8_t* w = a.Wq + (size_t)(tile_n0(j) + g) * K + kb0 + 64 * st + 16 * tq;
+                uint8_t* slot = slot_of(u);
+                cp_async16(slot, w);
+                cp_async16(slot + 512, w + (size_t)8 * K);
+            }
+        }
+    };
+    auto issue_x = [&](int u) {
+        if (u < total) {
+            const int st = u % nsteps;
+            if (step_ok(st)) {
+                uint8_t* slot = slot_of(u);
+#pragma unroll
+                for (int t = 0; t < MT; ++t)
+                    if (xok[t]) cp_async16(slot + 1024 + 512 * t, xp[t] + 64 * st);
+            }
+        }
+    };
+
+    // epilogue thread mapping: (row ri, tile column nl)
+    const int nl = tid & 15, ri = tid >> 4;
+    const bool active = ri < a.M;
+    // constant inputs may be read before the wait
+    float cs_next = WRITE_I32 ? 0.0f : a.col_scale[tile_n0(0) + nl];
+    pdl_trigger();
+#pragma unroll
+    for (int d = 0; d < R; ++d) {
+        issue_w(d);
+        cp_async_commit();
+    }
+    pdl_wait();
+#pragma unroll
+    for (int d = 0; d < R; ++d) issue_x(d);
+    cp_async_commit();
+    const float rs = (!WRITE_I32 && active) ? __ldcg(a.row_scale + ri) : 0.0f;
+
+    // A4 operands: indices requested together with the count (positions past it
+    // are loaded but not used)
+    const bool outl = !WRITE_I32 && a.use_outliers;
+    const int idx0 = (outl && tid < kTileOutChunk && tid < K) ? ldg_cg_s32(a.outlier_idx + tid) : 0;
+    const int cnt = outl ? ldg_cg_s32(&a.hdr->outlier_count) : 0;
+    const int cst = min(cnt, kTileOutChunk);
+    if (tid < kTileOutChunk) s_idx[tid] = idx0;
+    {
+        // the gathered X values are zero-padded past the count up to a multiple of 64
+        const int cv = (cst + 7) >> 3;
+        for (int e = tid; e < a.M * (kTileOutChunk / 8); e += kGemvWarps * 32) {
+            const int i = e / (kTileOutChunk / 8), qv = e - i * (kTileOutChunk / 8);
+            if (qv < cv) cp_async16(&s_xo[i][qv * 8], a.xo + (size_t)i * a.xo_pitch + qv * 8);
+        }
+    }
+    __syncthreads();  // s_idx
+    auto stage_w16 = [&](int buf, int n0) {
+        for (int e = tid; e < 2 * cst; e += kGemvWarps * 32) {
+            const int jx = e >> 1, hv = e & 1;
+            cp_async16(&s_w16o[buf][jx][hv * 8], a.W16 + (size_t)s_idx[jx] * a.N + n0 + hv * 8);
+        }
+        cp_async_commit();
+    };
+    stage_w16(0, tile_n0(0));
+
+    // Refill cursor: the step u + R as (tile jr, step sr of the warp's slice) and
+    // its weight source; the ring slot of step u is sl.  Both advance without
+    // divisions.  Steps [0, nfull) of a slice are whole 64-byte steps.
+    const int nfull = kend > kb0 ? (kend - kb0) >> 6 : 0;
+    uint8_t* const my_ring = ring + lane * 16;
+    int jr = nsteps > 0 ? R / nsteps : my_tiles, sr = nsteps > 0 ? R % nsteps : 0;
+    auto w_src = [&](int jt) { return a.Wq + (size_t)(tile_n0(jt) + g) * K + kb0 + 16 * tq; };
+    const int8_t* wr = jr < my_tiles ? w_src(jr) + 64 * sr : nullptr;
+    int sl = 0;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    int u = 0;
+    for (int j = 0; j < my_tiles; ++j) {
+        int acc[MT][4];
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[t][r] = 0;
+        for (int st = 0; st < nsteps; ++st, ++u) {
+            if (u == 0)
+                cp_async_wait_group<1>();      // the first R steps, both halves (staging may be pending)
+            else if (u >= R)
+                cp_async_wait_group<R - 1>();  // at least R - 1 groups followed the refill of step u
+            uint8_t* slot = my_ring + sl * SLOT;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(slot);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(slot + 512);
+            const bool ok = st < nfull || kb0 + st * 64 + 16 * tq < kend;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                const uint4 xf = (ok && xok[t]) ? *reinterpret_cast<const uint4*>(slot + 1024 + 512 * t) : z;
+                imma_16832(acc[t], w0.x, w1.x, w0.y, w1.y, xf.x, xf.y);
+                imma_16832(acc[t], w0.z, w1.z, w0.w, w1.w, xf.z, xf.w);
+            }
+            // the slot's values were consumed by the MMAs above: refill it with step u + R
+            if (jr < my_tiles && (sr < nfull || kb0 + sr * 64 + 16 * tq < kend)) {
+                cp_async16(slot, wr);
+                cp_async16(slot + 512, wr + (size_t)8 * K);
+#pragma unroll
+                for (int t = 0; t < MT; ++t)
+                    if (xok[t]) cp_async16(slot + 1024 + 512 * t, xp[t] + 64 * sr);
+            }
+            cp_async_commit();
+            wr += 64;
+            if (++sr == nsteps) {
+                sr = 0;
+                if (++jr < my_tiles) wr = w_src(jr);
+            }
+            sl = sl + 1 == R ? 0 : sl + 1;
+        }
+        // accumulator layout: d0,d1 -> (column g, x rows 8t+2q, +1); d2,d3 -> (column g+8, same rows)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            const int i0 = 8 * t + 2 * tq;
+            s_red[warp][i0][g] = acc[t][0];
+            s_red[warp][i0 + 1][g] = acc[t][1];
+            s_red[warp][i0][g + 8] = acc[t][2];
+            s_red[warp][i0 + 1][g + 8] = acc[t][3];
+        }
+        const float cs = cs_next;
+        if (!WRITE_I32 && j + 1 < my_tiles) cs_next = a.col_scale[tile_n0(j + 1) + nl];
+        // this tile's staging has landed once at most R - 1 groups are pending:
+        // the nsteps refill groups of the tile followed it
+        if (nsteps >= R - 1)
+            cp_async_wait_group<R - 1>();
+        else
+            cp_async_wait_all();
+        __syncthreads();  // partials and staged operands visible to all
+        // the other staging buffer was last read by the previous tile's
+        // epilogue, which every thread finished before the barrier ending it
+        if (j + 1 < my_tiles) stage_w16((j + 1) & 1, tile_n0(j + 1));
+
+        const int n = tile_n0(j) + nl;
+        int32_t c = 0;
+        if (active) {
+#pragma unroll
+            for (int w = 0; w < kGemvWarps; ++w) c += s_red[w][ri][nl];
+        }
+        if (WRITE_I32) {
+            if (active) reinterpret_cast<int32_t*>(a.out)[(size_t)ri * a.N + n] = c;
+        } else if (active) {
+            float f = 0.0f;
+            for (int jj = 0; jj < cst; ++jj)
+                f = fmaf(__half2float(s_xo[ri][jj]), __half2float(s_w16o[j & 1][jj][nl]), f);
+            for (int jj = cst; jj < cnt; ++jj) {  // past the staged chunk: through L2
+                const int k = __ldcg(a.outlier_idx + jj);
+                const __half xv = __ldcg(a.xo + (size_t)ri * a.xo_pitch + jj);
+                f = fmaf(__half2float(xv), __half2float(a.W16[(size_t)k * a.N + n]), f);
+            }
+            const float scale = rs * cs * (1.0f / 16129.0f);
+            reinterpret_cast<__half*>(a.out)[(size_t)ri * a.N + n] = __float2half_rn(fmaf((float)c, scale, f));
+        }
+        __syncthreads();  // s_red and this tile's staging buffer may be overwritten
+    }
+    cp_async_wait_all();  // no copy may still target shared memory when the CTA ends
 }
 
 }  // namespace llmint8

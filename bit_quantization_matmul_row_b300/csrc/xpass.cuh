@@ -60,6 +60,12 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 __global__ void __launch_bounds__(kScanThreads) k_outlier_scan(const __half* __restrict__ X, int M, int K, float t,
                                                                uint32_t* __restrict__ bitmap, WsHeader* hdr) {
     pdl_trigger();
+    if (gridDim.y == 1 && (threadIdx.x & 31) == 0 && blockIdx.x * kScanCols < K) {
+        // this CTA's X segments into L2 while the predecessor finishes
+        const uint32_t bytes = 2u * (uint32_t)min(kScanCols, K - (int)blockIdx.x * kScanCols);
+        for (int r = threadIdx.x >> 5; r < M; r += 8)
+            prefetch_l2_bulk(X + (size_t)r * K + (size_t)blockIdx.x * kScanCols, bytes);
+    }
     pdl_wait();
     if (hdr != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->status = 0u;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -171,6 +177,9 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
     // before any writes into its shared memory
     if (cflags) cluster_arrive_relaxed();
     pdl_trigger();
+    // this CTA's row of X into L2 while the predecessor finishes (32 KB per request)
+    for (int off = tid * 32768; off < 2 * K; off += kRowThreads * 32768)
+        prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.X + (size_t)row * K) + off, (uint32_t)min(32768, 2 * K - off));
     pdl_wait();
 
     const __half* xrow = a.X + (size_t)row * K;

@@ -55,6 +55,26 @@ def test_decode_long_k(M, K, N):
     check(X, W, 6.0)
 
 
+@pytest.mark.parametrize("M,K,extra_tiles,frac", [
+    (1, 1040, 1, 0.01),      # one CTA takes a second tile
+    (8, 4096, 150, 0.002),   # two tiles for half the CTAs; the 8-step ring wraps across tiles
+    (4, 1040, 400, 0.09),    # ragged K (warps 6, 7 have no steps), ~94 outliers: past the staged chunk
+    (1, 64, 600, 0.05),      # one K step: only warp 0 streams; three or four tiles per CTA
+    (4, 11008, 40, 0.001),
+    (16, 1040, 400, 0.05),   # more than 8 rows: one-tile CTAs in several waves
+])
+def test_decode_many_tiles(M, K, extra_tiles, frac):
+    # More 16-column tiles than two CTAs per SM.  Up to 8 rows of X this is the
+    # persistent GEMV (each CTA walks several tiles, its ring running on across
+    # them); compared in full.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N = 16 * (2 * sms + extra_tiles)
+    X, W = xw(M, K, N, frac=frac, seed=M * 7 + extra_tiles, min_count=3)
+    check(X, W, 6.0)
+    if extra_tiles == 1:
+        check(X, W, 6.0, int8_variant=True)  # no outlier slice (threshold +inf)
+
+
 @pytest.mark.parametrize("M,frac", [(1, 0.3), (4, 0.45), (16, 0.4)])
 def test_decode_outlier_chunks(M, frac):
     # 300-500 outlier columns: more than one 256-column chunk of the fp16 slice
