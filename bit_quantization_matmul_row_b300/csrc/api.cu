@@ -390,17 +390,25 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         if (st != LLMINT8_OK) return st;
     }
     if ((st = get_encoder()) != LLMINT8_OK) return st;
+    // CTA pairs (256 x 256 tiles, each CTA loading 128 columns of B) once M
+    // spans two 128-row tiles
+    const bool pair = M > kBM && dev->sms >= 2;
+    const int b_rows = pair ? kBN / 2 : kBN;
     CUtensorMap tm_a, tm_b, tm_xo, tm_wo;
     if ((st = encode_fp16_2d(&tm_a, w.codes, M, K, K, kBM)) != LLMINT8_OK) return st;
-    if ((st = encode_fp16_2d(&tm_b, Wq16, N, K, K, kBN)) != LLMINT8_OK) return st;
+    if ((st = encode_fp16_2d(&tm_b, Wq16, N, K, K, b_rows)) != LLMINT8_OK) return st;
     if ((st = encode_fp16_2d(&tm_xo, w.xo, M, L.kp, L.kp, kBM)) != LLMINT8_OK) return st;
-    if ((st = encode_fp16_2d(&tm_wo, w.w16o, N, L.kp, L.kp, kBN)) != LLMINT8_OK) return st;
+    if ((st = encode_fp16_2d(&tm_wo, w.w16o, N, L.kp, L.kp, b_rows)) != LLMINT8_OK) return st;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!dev->gemm_attr_set) {
-            if (cudaFuncSetAttribute(k_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(k_gemm_tc<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kGemmSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(k_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                cudaFuncSetAttribute(k_gemm_tc<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kGemmSmem) != cudaSuccess)
                 return LLMINT8_ECUDA;
             dev->gemm_attr_set = true;
@@ -418,12 +426,23 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
     // the int32 accumulator leaves the outlier slice out (it is not part of C)
     ga.use_outliers = (use_outliers && !write_i32) ? 1 : 0;
     ga.spin_limit = kDefaultSpinLimit;
+    if (pair) {
+        const int units = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
+        const int clusters = units < dev->sms / 2 ? units : dev->sms / 2;
+        const dim3 grid(2 * clusters);
+        if (write_i32)
+            return launch_cluster(k_gemm_tc<true, true>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u, tm_a, tm_b,
+                                  tm_xo, tm_wo, ga);
+        return launch_cluster(k_gemm_tc<false, true>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u, tm_a, tm_b,
+                              tm_xo, tm_wo, ga);
+    }
     const int ntiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     const int grid = ntiles < dev->sms ? ntiles : dev->sms;
     if (write_i32)
-        return launch(k_gemm_tc<true>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo, tm_wo,
-                      ga);
-    return launch(k_gemm_tc<false>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo, tm_wo, ga);
+        return launch(k_gemm_tc<true, false>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo,
+                      tm_wo, ga);
+    return launch(k_gemm_tc<false, false>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo,
+                  tm_wo, ga);
 }
 
 // Kernels one matmul call launches (the plan matmul_impl follows).

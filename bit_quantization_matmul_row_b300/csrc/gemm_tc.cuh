@@ -20,6 +20,19 @@
 //   warp 0      TMA producer: 4-stage ring of (A 128x64, B 256x64) fp16 tiles
 //   warp 1      TMEM owner and MMA issuer (one thread), M=128 N=256 K=16 MMAs
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).., column half (w-2)/4
+//
+// PAIR (M > 128): the CTAs run as clusters of two that compute 256 x 256 tiles
+// with tcgen05.mma.cta_group::2.  Each CTA loads its own 128 rows of A and its
+// 128 columns of B, so a ring stage is 32 KB instead of 48 KB and the same
+// shared memory holds 6 stages instead of 4.  The tensor core consumes a stage
+// in about 0.3 us; with 4 stages its issuer waited for data about a third of
+// the time (L2 latency under load), 6 stages cover 1.5 times as much.  Both
+// producers' copies complete on the first CTA's full barrier (TMA
+// .cta_group::2; that CTA registers the bytes of both), its MMA
+// thread issues the M=256 N=256 MMAs, and its commits arrive on the empty and
+// TMEM-full barriers of both CTAs (multicast).  Each CTA's epilogue drains its
+// own TMEM (rows 0..127 of the pair tile in the first CTA, 128..255 in the
+// second) and releases a TMEM buffer on the first CTA's barrier.
 #pragma once
 
 #include "common.cuh"
@@ -28,13 +41,17 @@
 namespace llmint8 {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 4;      // one CTA per tile: 48 KB stages
+constexpr int kPairStages = 6;  // CTA pairs: 32 KB stages
+constexpr int kMaxStages = kPairStages;
 constexpr int kChunkSteps = 16;  // 16 x 64 = 1024 products per exact fp32 chunk
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kStageA = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kStageB = kBN * kBK * 2;  // 32 KB
+constexpr uint32_t kPairStageB = kStageB / 2;  // 16 KB: the CTA's half of the B tile
 constexpr uint32_t kTmemCols = 512;          // two 256-column fp32 accumulators
+static_assert(kStages * (kStageA + kStageB) == kPairStages * (kStageA + kPairStageB), "same ring size");
 constexpr size_t kGemmSmem = 1024 /*align slack*/ + (size_t)kStages * (kStageA + kStageB) + 256;
 
 struct GemmArgs {
@@ -49,8 +66,8 @@ struct GemmArgs {
 };
 
 struct GemmSmem {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t teardown;
@@ -58,20 +75,30 @@ struct GemmSmem {
     uint32_t abort_flag;
 };
 
-template <bool WRITE_I32>
+template <bool WRITE_I32, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_wo, GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int S = PAIR ? kPairStages : kStages;
+    constexpr uint32_t SB = PAIR ? kPairStageB : kStageB;  // B bytes of a stage in this CTA
     uint8_t* stage_a = smem;
-    uint8_t* stage_b = smem + kStages * kStageA;
-    GemmSmem* ss = reinterpret_cast<GemmSmem*>(smem + kStages * (kStageA + kStageB));
+    uint8_t* stage_b = smem + S * kStageA;
+    GemmSmem* ss = reinterpret_cast<GemmSmem*>(smem + S * (kStageA + SB));
     volatile uint32_t* abort_flag = &ss->abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_m = (a.M + kBM - 1) / kBM, tiles_n = (a.N + kBN - 1) / kBN;
+    // work units: 128 x 256 tiles, or 256 x 256 tiles of a CTA pair
+    const uint32_t rank = PAIR ? cluster_cta_rank() : 0u;
+    const int unit_rows = PAIR ? 2 * kBM : kBM;
+    const int tiles_m = (a.M + unit_rows - 1) / unit_rows, tiles_n = (a.N + kBN - 1) / kBN;
     const int ntiles = tiles_m * tiles_n;
+    const int unit0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+    const int ustride = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
+    // this CTA's first row in unit row tm and first column of its B half
+    auto row_of = [&](int tm) { return tm * unit_rows + (int)rank * kBM; };
+    auto bcol_of = [&](int tn) { return tn * kBN + (int)rank * (kBN / 2); };
     const int ksteps = (a.K + kBK - 1) / kBK;
     const int nchunks_int = (ksteps + kChunkSteps - 1) / kChunkSteps;
 
@@ -79,13 +106,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // dependent launch); everything after pdl_wait() may read its results
     pdl_trigger();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&ss->full[s], 1);
             mbar_init(&ss->empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ss->tmem_full[b], 1);
-            mbar_init(&ss->tmem_empty[b], kEpiWarps);
+            mbar_init(&ss->tmem_empty[b], PAIR ? 2 * kEpiWarps : kEpiWarps);
         }
         mbar_init(&ss->teardown, 1);
         ss->abort_flag = 0;
@@ -98,17 +125,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     }
     if (warp == 1) {
-        tmem_alloc(&ss->tmem_base, kTmemCols);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(&ss->tmem_base, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&ss->tmem_base, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers initialised before any remote arrive
     tc_fence_after();
+    // barriers of the pair's first CTA, as shared::cluster addresses
+    const uint32_t lead_full0 = PAIR ? mapa_shared(smem_u32(&ss->full[0]), 0) : 0u;
+    const uint32_t lead_tmem_empty0 = PAIR ? mapa_shared(smem_u32(&ss->tmem_empty[0]), 0) : 0u;
     const uint32_t tmem_base = ss->tmem_base;
     pdl_wait();
     const int n_out = a.use_outliers ? __ldcg(&a.hdr->outlier_count) : 0;
     const int osteps = (n_out + kBK - 1) / kBK;
 
+    auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return mbar_wait_bounded(bar, parity, a.spin_limit, abort_flag);
+    };
     auto fail = [&](uint32_t where) {
         *abort_flag = 1u;
         record_error(a.err, kStatusTimeout, where);
@@ -117,7 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // warp is converged again for the .sync.aligned TMEM loads that follow
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         uint32_t got = 0;
-        if (lane == 0) got = mbar_wait_bounded(bar, parity, a.spin_limit, abort_flag) ? 1u : 0u;
+        if (lane == 0) got = wait_bar(bar, parity) ? 1u : 0u;
         got = __shfl_sync(0xffffffffu, got, 0);
         return got != 0;
     };
@@ -127,52 +166,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_parity[kStages];
-            bool issued[kStages];
-            for (int s = 0; s < kStages; ++s) issued[s] = false, issued_parity[s] = 0;
+            uint32_t issued_parity[S];
+            bool issued[S];
+            for (int s = 0; s < S; ++s) issued[s] = false, issued_parity[s] = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            for (int tile = unit0; tile < ntiles && ok; tile += ustride) {
                 const int tm = tile % tiles_m, tn = tile / tiles_m;
                 const int total = ksteps + osteps;
                 for (int s = 0; s < total; ++s) {
-                    if (!mbar_wait_bounded(&ss->empty[stage], phase ^ 1u, a.spin_limit, abort_flag)) {
+                    if (!wait_bar(&ss->empty[stage], phase ^ 1u)) {
                         fail(1);
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&ss->full[stage], kStageA + kStageB);
-                    if (s < ksteps) {
-                        tma_load_2d(stage_a + stage * kStageA, &tm_a, &ss->full[stage], s * kBK, tm * kBM);
-                        tma_load_2d(stage_b + stage * kStageB, &tm_b, &ss->full[stage], s * kBK, tn * kBN);
+                    const bool main_k = s < ksteps;
+                    const int kx = (main_k ? s : s - ksteps) * kBK;
+                    const void* ta = main_k ? (const void*)&tm_a : (const void*)&tm_xo;
+                    const void* tb = main_k ? (const void*)&tm_b : (const void*)&tm_wo;
+                    if constexpr (PAIR) {
+                        // this CTA's rows of A and columns of B, signalled on the first CTA's
+                        // barrier, where the first CTA alone registers both CTAs' bytes (the
+                        // other CTA's copies may land first: the transaction count of the
+                        // phase goes negative until the arrival, which completes nothing)
+                        const uint32_t fb = lead_full0 + (uint32_t)stage * 8u;
+                        if (rank == 0) mbar_arrive_expect_tx(&ss->full[stage], 2 * (kStageA + SB));
+                        tma_load_2d_pair(stage_a + stage * kStageA, ta, fb, kx, row_of(tm));
+                        tma_load_2d_pair(stage_b + stage * SB, tb, fb, kx, bcol_of(tn));
                     } else {
-                        const int so = s - ksteps;
-                        tma_load_2d(stage_a + stage * kStageA, &tm_xo, &ss->full[stage], so * kBK, tm * kBM);
-                        tma_load_2d(stage_b + stage * kStageB, &tm_wo, &ss->full[stage], so * kBK, tn * kBN);
+                        mbar_arrive_expect_tx(&ss->full[stage], kStageA + SB);
+                        tma_load_2d(stage_a + stage * kStageA, ta, &ss->full[stage], kx, tm * kBM);
+                        tma_load_2d(stage_b + stage * SB, tb, &ss->full[stage], kx, tn * kBN);
                     }
                     issued[stage] = true;
                     issued_parity[stage] = phase;
-                    if (++stage == kStages) stage = 0, phase ^= 1u;
+                    if (++stage == S) stage = 0, phase ^= 1u;
                 }
             }
-            if (!ok) {
+            if (!ok && !PAIR) {
                 // let copies already in flight land before the CTA can exit
-                for (int s = 0; s < kStages; ++s)
+                // (pairs: they signal the first CTA, which keeps running until
+                // the cluster barrier at the end)
+                for (int s = 0; s < S; ++s)
                     if (issued[s]) mbar_wait_bounded(&ss->full[s], issued_parity[s], 1u << 20, nullptr);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc_f16(kBM, kBN);
+        // (pairs: the first CTA's thread issues for both)
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = make_idesc_f16(PAIR ? 2 * kBM : kBM, kBN);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t chunk = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            for (int tile = unit0; tile < ntiles && ok; tile += ustride) {
                 const int nchunks = nchunks_int + (osteps ? 1 : 0);
                 for (int ch = 0; ch < nchunks && ok; ++ch, ++chunk) {
                     const uint32_t b = chunk & 1u, use = (chunk >> 1) & 1u;
-                    if (!mbar_wait_bounded(&ss->tmem_empty[b], use ^ 1u, a.spin_limit, abort_flag)) {
+                    if (!wait_bar(&ss->tmem_empty[b], use ^ 1u)) {
                         fail(2);
                         ok = false;
                         break;
@@ -182,28 +233,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int s_end = ch < nchunks_int ? min(ksteps, s_begin + kChunkSteps) : ksteps + osteps;
                     const uint32_t d_tmem = tmem_base + b * (uint32_t)kBN;
                     for (int s = s_begin; s < s_end; ++s) {
-                        if (!mbar_wait_bounded(&ss->full[stage], phase, a.spin_limit, abort_flag)) {
+                        if (!wait_bar(&ss->full[stage], phase)) {
                             fail(3);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint64_t ad = make_sdesc_k128(smem_u32(stage_a + stage * kStageA));
-                        const uint64_t bd = make_sdesc_k128(smem_u32(stage_b + stage * kStageB));
+                        const uint64_t bd = make_sdesc_k128(smem_u32(stage_b + stage * SB));
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
                             // advance 16 fp16 = 32 bytes inside the 128-byte swizzled row
-                            tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
-                                       (s > s_begin || kk > 0) ? 1u : 0u);
+                            const uint32_t acc = (s > s_begin || kk > 0) ? 1u : 0u;
+                            if constexpr (PAIR)
+                                tc_mma_f16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, acc);
+                            else
+                                tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, acc);
                         }
-                        tc_commit(&ss->empty[stage]);
-                        if (++stage == kStages) stage = 0, phase ^= 1u;
+                        if constexpr (PAIR)
+                            tc_commit_pair(&ss->empty[stage], 0x3);  // both CTAs' stage is free
+                        else
+                            tc_commit(&ss->empty[stage]);
+                        if (++stage == S) stage = 0, phase ^= 1u;
                     }
-                    if (ok) tc_commit(&ss->tmem_full[b]);
+                    if (ok) {
+                        if constexpr (PAIR)
+                            tc_commit_pair(&ss->tmem_full[b], 0x3);
+                        else
+                            tc_commit(&ss->tmem_full[b]);
+                    }
                 }
             }
             // all issued MMAs complete before TMEM can be released
-            tc_commit(&ss->teardown);
+            if constexpr (PAIR)
+                tc_commit_pair(&ss->teardown, 0x1);
+            else
+                tc_commit(&ss->teardown);
             mbar_wait_bounded(&ss->teardown, 0, a.spin_limit, nullptr);
         }
     } else {
@@ -214,9 +279,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t chunk = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        // release a TMEM buffer: on this CTA's barrier, or the first CTA's for pairs
+        auto release = [&](uint32_t b) {
+            if constexpr (PAIR)
+                mbar_arrive_cluster(lead_tmem_empty0 + b * 8u);
+            else
+                mbar_arrive(&ss->tmem_empty[b]);
+        };
+        for (int tile = unit0; tile < ntiles && ok; tile += ustride) {
             const int tm = tile % tiles_m, tn = tile / tiles_m;
-            const int row = tm * kBM + q * 32 + lane;
+            const int row = row_of(tm) + q * 32 + lane;
             const int col0 = tn * kBN + h * 128;
             int32_t sum[128];
 #pragma unroll
@@ -240,7 +312,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ss->tmem_empty[b]);
+                if (lane == 0) release(b);
             }
             if (!ok) break;
             uint32_t fb = 0;
@@ -305,7 +377,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (has_f) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ss->tmem_empty[fb]);
+                if (lane == 0) release(fb);
                 ++chunk;
             }
         }
@@ -313,10 +385,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    // pairs: the first CTA's MMAs into both TMEMs have completed (its issuer
+    // waited for the teardown commit) before either CTA frees its columns
+    if constexpr (PAIR) cluster_sync_all();
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
