@@ -271,10 +271,14 @@ def run_ours(args, world, rank, local):
 
     ncase = len(cases)
     # kernels per call (outlier scan, row quantization, GEMV) as the library plans them
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for d in cases:
         c = d["c"]
         d["kpc"] = api.llmint8_kernels_per_call(c.M, c.K, c.N, c.threshold)
+        # one GEMV family (same sources): one-tile CTAs, or the persistent form when
+        # up to 8 rows meet more 16-column tiles than two CTAs per SM
         d["kernel"] = "k_gemv_decode"
+        d["form"] = "k_gemv_decode_tiles" if c.M <= 8 and c.N // 16 > 2 * sms else "k_gemv_decode"
     launches_per_step = sum(d["kpc"] for d in cases)
 
     # ---- one CUDA graph per step (the 9 llmint8_matmul calls), so the GPU is not
@@ -342,7 +346,7 @@ def run_ours(args, world, rank, local):
         elapsed_ms = float(t.item())
     total_bytes = step_bytes * args.steps * world
     value = total_bytes / (elapsed_ms * 1e-3) / 1e9
-    per_shape = [{"M": d["c"].M, "K": d["c"].K, "N": d["c"].N, "outliers": d["n_o"], "kernel": d["kernel"],
+    per_shape = [{"M": d["c"].M, "K": d["c"].K, "N": d["c"].N, "outliers": d["n_o"], "kernel": d["form"],
                   "kernel_us": 1e3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G,
                   "kernel_gbs": d["bytes"] / (1e-3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G) / 1e9}
                  for ci, d in enumerate(cases)]
