@@ -67,8 +67,9 @@ def _load():
             lib.oracle_int8_matmul.argtypes = [P, P, I, I, I, P, ctypes.c_int]
             lib.oracle_outlier_matmul.argtypes = [P, P, P, I, I, I, P, ctypes.c_int]
             lib.oracle_merge.argtypes = [P, P, P, P, I, I, P]
+            lib.oracle_dequantize_weight.argtypes = [P, P, I, I, P]
             for f in ("oracle_quantize_weight", "oracle_outlier_columns", "oracle_quantize_rows",
-                      "oracle_quantize_per_tensor",
+                      "oracle_quantize_per_tensor", "oracle_dequantize_weight",
                       "oracle_int8_matmul", "oracle_outlier_matmul", "oracle_merge"):
                 getattr(lib, f).restype = None
             _lib = lib
@@ -210,13 +211,23 @@ def per_tensor_int8_matmul(X: np.ndarray, W: np.ndarray, nthreads: int | None = 
     return merge(C, np.full(M, sx, np.float32), np.full(N, sw, np.float32), None)
 
 
+def dequantize_weight(Wq: np.ndarray, s_w: np.ndarray) -> np.ndarray:
+    """A4 weight rows when only the int8 codes are kept: fp16(q * (s_w / 127)) [K,N]."""
+    Wq = np.ascontiguousarray(Wq, np.int8)
+    K, N = Wq.shape
+    sw = np.ascontiguousarray(s_w, np.float32)
+    out = np.empty((K, N), np.uint16)
+    _load().oracle_dequantize_weight(_ptr(Wq), _ptr(sw), K, N, _ptr(out))
+    return out.view(np.float16)
+
+
 def outlier_indices(is_outlier: np.ndarray) -> np.ndarray:
     """Sorted int32 indices of the outlier columns."""
     return np.flatnonzero(np.asarray(is_outlier)).astype(np.int32)
 
 
 def llmint8_matmul(X: np.ndarray, W: np.ndarray, t: float, rows=None, nthreads: int | None = None,
-                   wq=None, cols=None):
+                   wq=None, cols=None, w16_rows=None):
     """The whole path A0..A5 for Y = X.W with threshold t.
 
     Outlier detection (A1) always scans all rows of X, because the outlier set
@@ -225,8 +236,10 @@ def llmint8_matmul(X: np.ndarray, W: np.ndarray, t: float, rows=None, nthreads: 
     ``cols`` (optional) restricts the output columns: A0 (one scale per output
     column), A3, A4 and A5 are each local to a column, so the oracle simply
     runs on W[:, cols].  ``wq`` may pass a precomputed (Wq, s_w) from
-    quantize_weight of the (restricted) W.  Returns a dict with every
-    intermediate.
+    quantize_weight of the (restricted) W.  ``w16_rows`` (optional index
+    array) selects the mode where only those rows of W are kept in fp16: A4
+    then takes every other outlier row from dequantize_weight.  Returns a dict
+    with every intermediate.
     """
     if cols is not None:
         W = np.ascontiguousarray(W[:, np.asarray(cols)])
@@ -235,7 +248,12 @@ def llmint8_matmul(X: np.ndarray, W: np.ndarray, t: float, rows=None, nthreads: 
     Xs = X if rows is None else np.ascontiguousarray(X[np.asarray(rows)])
     Xq, s_x = quantize_rows(Xs, is_out)
     C = int8_matmul(Xq, Wq, nthreads)
-    F = outlier_matmul(Xs, W, is_out, nthreads) if is_out.any() else np.zeros(C.shape, np.float64)
+    W4 = W
+    if w16_rows is not None:  # fp16 rows only where kept, dequantized codes elsewhere
+        keep = np.zeros(W.shape[0], bool)
+        keep[np.asarray(w16_rows, np.int64)] = True
+        W4 = np.where(keep[:, None], W, dequantize_weight(Wq, s_w))
+    F = outlier_matmul(Xs, W4, is_out, nthreads) if is_out.any() else np.zeros(C.shape, np.float64)
     Y = merge(C, s_x, s_w, F)
     return dict(Y=Y, C=C, F=F, Xq=Xq, s_x=s_x, Wq=Wq, s_w=s_w, is_outlier=is_out,
                 outliers=outlier_indices(is_out))

@@ -308,6 +308,27 @@ void oracle_outlier_matmul(const uint16_t *X, const uint16_t *W, const uint8_t *
 }
 
 /* ---------------------------------------------------------------------------
+ * A4 without a full fp16 copy of W: the dequantized weight.  Dequantization
+ * multiplies a code by its scale ([PITFALLS] section 1 recovers the values
+ * from the codes; [FABRIC] section 2.2: one scale per output column), here
+ * absmax/127 since the scale is stored as the absmax.  When only the int8
+ * codes of W are kept, an outlier row k of W is taken as
+ *   w_hat[k,n] = fp16( fp32(q[k,n]) * fp32(s_w[n] / 127) ),
+ * each fp32 operation rounded once to nearest even, then rounded to fp16 (the
+ * operand precision of the outlier product).  s_w = 0 gives 0.
+ * ------------------------------------------------------------------------- */
+void oracle_dequantize_weight(const int8_t *Wq, const float *s_w, int64_t K, int64_t N, uint16_t *W_hat)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        float r = s_w[n] / 127.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float p = (float)Wq[k * N + n] * r;
+            W_hat[k * N + n] = oracle_double_to_half((double)p);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------
  * A5. Dequantize and merge ([PITFALLS] section 3.3: dequantize the 8-bit result,
  * then ADD the 16-bit result; [FABRIC] section 2.2: rescale the integer result
  * by scale_x * scale_w).  With s_x and s_w stored as absmax values, each code

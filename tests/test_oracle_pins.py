@@ -348,3 +348,59 @@ def test_without_outliers_the_decomposition_is_plain_int8(oracle_mod):
     exact = X.astype(np.float64) @ W.astype(np.float64)
     err = lambda Y: np.linalg.norm(Y.astype(np.float64) - exact) / np.linalg.norm(exact)
     assert err(y_naive) <= err(oracle_mod.per_tensor_int8_matmul(X, W))
+
+
+# ---------------------------------------------------------------------------------
+# A4 without a full fp16 copy of W: dequantized int8 weight rows
+# ---------------------------------------------------------------------------------
+
+def test_dequantized_weight_matches_worked_example(oracle_mod):
+    # The page dequantizes the codes [1, 3, -4, 127] of scale 12 back to the
+    # printed [0.09, 0.28, -0.38, 12.0]; the dequantized weight rows follow the
+    # same rule (code times absmax / 127).
+    g = _read_golden("worked_example.txt")
+    W = np.array(g["values"], np.float16).reshape(4, 1)
+    Wq, sw = oracle_mod.quantize_weight(W)
+    w_hat = oracle_mod.dequantize_weight(Wq, sw)[:, 0].astype(np.float64)
+    assert [round(v, 2) for v in w_hat] == g["dequantized_2dp"]
+
+
+def test_dequantized_weight_error_bound_and_argmax(oracle_mod):
+    # Each dequantized weight is within half a code step (absmax / 254) plus one
+    # fp16 rounding of the original value, and the row holding a column's
+    # absmax dequantizes back to exactly that fp16 value (code +-127).
+    rng = np.random.default_rng(11)
+    W = (rng.standard_normal((256, 96)) * 0.02).astype(np.float16)
+    W[:, 5] = 0
+    W[7, 9] = 3.0
+    Wq, sw = oracle_mod.quantize_weight(W)
+    w_hat = oracle_mod.dequantize_weight(Wq, sw).astype(np.float64)
+    w = W.astype(np.float64)
+    bound = sw.astype(np.float64)[None, :] / 254.0 + fp16_ulp(w_hat) / 2 + 1e-12
+    assert np.all(np.abs(w_hat - w) <= bound)
+    arg = np.argmax(np.abs(w), axis=0)
+    cols = np.arange(w.shape[1])
+    nz = sw > 0
+    assert np.array_equal(w_hat[arg[nz], cols[nz]], w[arg[nz], cols[nz]])
+    assert not w_hat[:, 5].any()  # zero column: scale 0, weights 0
+
+
+def test_all_rows_kept_in_fp16_is_the_standard_path(oracle_mod):
+    rng = np.random.default_rng(12)
+    X = rng.standard_normal((9, 192)).astype(np.float16)
+    X[:, [3, 70, 150]] *= 30
+    W = (rng.standard_normal((192, 64)) * 0.02).astype(np.float16)
+    full = oracle_mod.llmint8_matmul(X, W, 6.0)
+    kept = oracle_mod.llmint8_matmul(X, W, 6.0, w16_rows=np.arange(192))
+    assert np.array_equal(full["Y"].view(np.uint16), kept["Y"].view(np.uint16))
+    assert np.array_equal(full["F"], kept["F"])
+    # Only the outlier slice depends on which rows are kept: no rows kept
+    # changes F (the weights of the outlier rows become their dequantized codes)
+    # and leaves the int8 part alone.
+    none = oracle_mod.llmint8_matmul(X, W, 6.0, w16_rows=np.array([], np.int64))
+    assert np.array_equal(none["C"], full["C"]) and np.array_equal(none["s_x"], full["s_x"])
+    assert not np.array_equal(none["F"], full["F"])
+    # without outliers the mode changes nothing
+    a = oracle_mod.llmint8_matmul(X, W, math.inf)
+    b = oracle_mod.llmint8_matmul(X, W, math.inf, w16_rows=np.array([], np.int64))
+    assert np.array_equal(a["Y"].view(np.uint16), b["Y"].view(np.uint16))
