@@ -19,6 +19,8 @@ EXPORTS = (
     "llmint8_workspace_bytes",
     "llmint8_matmul",
     "llmint8_matmul_int8",
+    "llmint8_matmul_w8",
+    "llmint8_pack_w16_rows",
     "llmint8_matmul_i32",
     "llmint8_xpass",
     "llmint8_gemm",
@@ -54,6 +56,8 @@ def load() -> ctypes.CDLL:
         lib.llmint8_workspace_bytes.restype = Z
         lib.llmint8_matmul.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_int8.argtypes = [P, I, I, I, P, P, P, P, P, Z, P]
+        lib.llmint8_matmul_w8.argtypes = [P, I, I, I, F, P, P, P, P, P, I, P, P, Z, P]
+        lib.llmint8_pack_w16_rows.argtypes = [P, I, I, P, I, P, P, P]
         lib.llmint8_matmul_i32.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
         lib.llmint8_xpass.argtypes = [P, I, I, I, F, P, Z, P]
         lib.llmint8_gemm.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
@@ -64,6 +68,7 @@ def load() -> ctypes.CDLL:
         lib.llmint8_device_status.argtypes = [P, P]
         lib.llmint8_selftest_timeout.argtypes = [P, I, P]
         for f in ("llmint8_quantize_weight", "llmint8_matmul", "llmint8_matmul_int8", "llmint8_matmul_i32",
+                  "llmint8_matmul_w8", "llmint8_pack_w16_rows",
                   "llmint8_xpass", "llmint8_gemm", "llmint8_matmul_noalloc", "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
             getattr(lib, f).restype = I
         _lib = lib

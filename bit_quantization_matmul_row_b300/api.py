@@ -118,6 +118,40 @@ def llmint8_matmul(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspace=Non
     return Y
 
 
+def llmint8_pack_w16_rows(W16, rows, stream=None):
+    """Kept fp16 rows of W for llmint8_matmul_w8: (W16c [R, N], row_map int32 [K])."""
+    K, N = W16.shape
+    _need(W16, torch.float16, (K, N), "W16")
+    rows = torch.as_tensor(rows, dtype=torch.int32, device=W16.device).contiguous()
+    R = rows.numel()
+    W16c = torch.empty((R, N), dtype=torch.float16, device=W16.device)
+    row_map = torch.empty((K,), dtype=torch.int32, device=W16.device)
+    st = _lib.load().llmint8_pack_w16_rows(_ptr(W16), K, N, _ptr(rows) if R else None, R,
+                                           _ptr(W16c) if R else None, _ptr(row_map), _stream(stream, W16))
+    _check(st, "llmint8_pack_w16_rows")
+    return W16c, row_map
+
+
+def llmint8_matmul_w8(X, threshold, Wq, colScaleW, Wq16, W16c=None, row_map=None, Y=None, workspace=None,
+                      stream=None):
+    """A1..A5 without a full fp16 copy of W: outlier rows from W16c via row_map, else dequantized codes."""
+    M, K, N = _shapes(X, Wq)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    if workspace is None:
+        workspace = make_workspace(M, K, N, X.device)
+    _need(X, torch.float16, (M, K), "X")
+    _need(Y, torch.float16, (M, N), "Y")
+    _need(row_map, torch.int32, (K,), "row_map")
+    R = 0 if W16c is None else W16c.shape[0]
+    _need(W16c, torch.float16, (R, N), "W16c")
+    st = _lib.load().llmint8_matmul_w8(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
+                                       _ptr(W16c) if R else None, _ptr(row_map), R, _ptr(Y), _ptr(workspace),
+                                       workspace.numel(), _stream(stream, X))
+    _check(st, "llmint8_matmul_w8")
+    return Y
+
+
 def llmint8_matmul_int8(X, Wq, colScaleW, Wq16, Y=None, workspace=None, stream=None):
     """Plain vector-wise int8 (threshold = +inf, no fp16 weight)."""
     M, K, N = _shapes(X, Wq)

@@ -191,13 +191,24 @@ llmint8_status check_common(const void* X, int M, int K, int N, float threshold,
     return LLMINT8_OK;
 }
 
+// Where the outlier slice (A4) reads the rows of W: the full fp16 copy W16, or
+// (w8) kept rows W16c through row_map and the dequantized codes for the rest.
+struct W16Src {
+    bool w8 = false;
+    const __half* W16c = nullptr;
+    const int32_t* row_map = nullptr;
+    int rows = 0;
+};
+
 // Checks of the GEMM operands.
 llmint8_status check_operands(int M, float threshold, const int8_t* Wq, const float* colScaleW, const void* Wq16,
-                              const void* W16, const void* out, bool write_i32) {
+                              const void* W16, const void* out, bool write_i32, const W16Src& src = W16Src()) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
     const bool decode = M <= LLMINT8_DECODE_MAX_M;
     if (!Wq || !colScaleW || !out) return LLMINT8_EINVAL;
-    if (use_outliers && !W16 && !write_i32) return LLMINT8_EINVAL;
+    if (use_outliers && !W16 && !write_i32 && !src.w8) return LLMINT8_EINVAL;
+    if (src.w8 && (src.rows < 0 || (src.rows > 0 && (!src.W16c || !src.row_map)))) return LLMINT8_EINVAL;
+    if (src.w8 && src.W16c && !aligned16(src.W16c)) return LLMINT8_EALIGN;
     if (!decode && !Wq16) return LLMINT8_EINVAL;
     if (!aligned16(Wq) || !aligned16(colScaleW) || !aligned16(out) || (Wq16 && !aligned16(Wq16)) ||
         (W16 && !aligned16(W16)))
@@ -321,7 +332,7 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
 llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
                            const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
                            void* workspace, const Layout& L, DeviceInfo* dev, cudaStream_t s,
-                           bool w16o_ready = false) {
+                           bool w16o_ready = false, const W16Src& src = W16Src()) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
     const WsView w(workspace, L);
     llmint8_status st;
@@ -344,6 +355,10 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         const int ksteps = (K + 63) / 64;
         ga.k_per_warp = ((ksteps + kGemvWarps - 1) / kGemvWarps) * 64;
         ga.use_outliers = use_outliers ? 1 : 0;
+        ga.w8 = src.w8 ? 1 : 0;
+        ga.W16c = src.W16c;
+        ga.row_map = src.row_map;
+        ga.w16_rows = src.rows;
         {
             std::lock_guard<std::mutex> lock(g_mu);
             if (!dev->gemv_attr_set) {
@@ -385,8 +400,10 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
 
     // A4 operand: gathered, transposed outlier rows of W16 (unless the X pass wrote it)
     if (use_outliers && !write_i32 && !w16o_ready) {
+        const W8Rows w8{src.W16c, src.row_map, src.rows, Wq, K, colScaleW};
         st = launch(k_gather_w16_outlier_rows, dim3((N + 63) / 64), dim3(256), 0, s, true,
-                    static_cast<const __half*>(W16), N, (const WsHeader*)w.hdr, (const int32_t*)w.idx, w.w16o, L.kp);
+                    src.w8 ? nullptr : static_cast<const __half*>(W16), N, (const WsHeader*)w.hdr,
+                    (const int32_t*)w.idx, w.w16o, L.kp, w8);
         if (st != LLMINT8_OK) return st;
     }
     if ((st = get_encoder()) != LLMINT8_OK) return st;
@@ -460,17 +477,19 @@ int kernels_per_call(int M, int K, int N, float threshold, bool write_i32) {
 
 llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
                            const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
-                           void* workspace, size_t ws_bytes, void* stream) {
+                           void* workspace, size_t ws_bytes, void* stream, const W16Src& src = W16Src()) {
     Layout L;
     DeviceInfo* dev = nullptr;
     llmint8_status st = check_common(X, M, K, N, threshold, workspace, ws_bytes, &L, &dev);
     if (st != LLMINT8_OK) return st;
-    if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, out, write_i32)) != LLMINT8_OK) return st;
+    if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, out, write_i32, src)) != LLMINT8_OK) return st;
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool gw = rowq_gathers_w16(L.decode, K, threshold, write_i32, W16);
+    // the row quantization gathers only from a full fp16 copy (W16 is null in w8 mode)
+    const bool gw = !src.w8 && rowq_gathers_w16(L.decode, K, threshold, write_i32, W16);
     if ((st = xpass_launch(X, M, K, threshold, workspace, L, dev, s, W16, N, gw)) != LLMINT8_OK) return st;
-    return gemm_launch(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, out, write_i32, workspace, L, dev, s, gw);
+    return gemm_launch(X, M, K, N, threshold, Wq, colScaleW, Wq16, src.w8 ? nullptr : W16, out, write_i32, workspace,
+                       L, dev, s, gw, src);
 }
 
 // Waits on a barrier nothing completes, bounded by spin_limit polls, then
@@ -539,6 +558,38 @@ llmint8_status llmint8_matmul(const void* X, int M, int K, int N, float threshol
                               size_t workspace_bytes, void* stream) {
     return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, workspace_bytes,
                        stream);
+}
+
+llmint8_status llmint8_matmul_w8(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
+                                 const float* colScaleW, const void* Wq16, const void* W16c, const int32_t* row_map,
+                                 int w16_rows, void* Y, void* workspace, size_t workspace_bytes, void* stream) {
+    W16Src src;
+    src.w8 = true;
+    src.W16c = static_cast<const __half*>(W16c);
+    src.row_map = row_map;
+    src.rows = w16_rows;
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, nullptr, Y, false, workspace, workspace_bytes,
+                       stream, src);
+}
+
+llmint8_status llmint8_pack_w16_rows(const void* W16, int K, int N, const int32_t* rows, int w16_rows, void* W16c,
+                                     int32_t* row_map, void* stream) {
+    if (!W16 || !row_map || K <= 0 || N <= 0 || K > kMaxK || w16_rows < 0 ||
+        (w16_rows > 0 && (!rows || !W16c)))
+        return LLMINT8_EINVAL;
+    if ((N % 16) || !aligned16(W16) || (W16c && !aligned16(W16c))) return LLMINT8_EALIGN;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = current_device(&dev);
+    if (st != LLMINT8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int gk = (K + 255) / 256;
+    if ((st = launch(k_row_map_clear, dim3(gk < 1024 ? gk : 1024), dim3(256), 0, s, false, row_map, K)) != LLMINT8_OK)
+        return st;
+    if (w16_rows == 0) return LLMINT8_OK;
+    const size_t work = (size_t)w16_rows * (N / 8);
+    const size_t gp = (work + 255) / 256;
+    return launch(k_pack_w16_rows, dim3(gp < 4096 ? (unsigned)gp : 4096u), dim3(256), 0, s, false,
+                  static_cast<const __half*>(W16), K, N, rows, w16_rows, static_cast<__half*>(W16c), row_map);
 }
 
 llmint8_status llmint8_matmul_int8(const void* X, int M, int K, int N, const int8_t* Wq, const float* colScaleW,

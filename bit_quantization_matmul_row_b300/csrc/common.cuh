@@ -99,6 +99,13 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
 
+// A4 weight without a full fp16 copy of W: code q of a column whose absmax is
+// s_w, dequantized as fp16(fp32(q) * fp32(s_w / 127)), each step rounded to
+// nearest even (a code times its scale, the scale stored as the absmax).
+__device__ __forceinline__ __half dequant_weight(int8_t q, float s_w) {
+    return __float2half_rn(__fmul_rn((float)q, __fdiv_rn(s_w, 127.0f)));
+}
+
 // Hint: bring [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
 // It moves nothing into the SM, so it may precede griddepcontrol.wait even for
 // data the predecessor writes: every read after the wait goes through L2, which

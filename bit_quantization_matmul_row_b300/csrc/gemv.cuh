@@ -60,7 +60,68 @@ struct GemvArgs {
     int M, K, N;
     int k_per_warp;             // multiple of 64
     int use_outliers;           // 0 when the threshold is +inf
+    // w8 = 1: no full fp16 copy of W (W16 unused).  Row k of W for the outlier
+    // slice is W16c[row_map[k]] when 0 <= row_map[k] < w16_rows, else the
+    // dequantized codes Wq[., k] with the column scales.
+    int w8;
+    const __half* W16c;         // [w16_rows, N] kept fp16 rows of W
+    const int32_t* row_map;     // [K] (nullptr: no row kept)
+    int w16_rows;
 };
+
+// Columns nb .. nb+7 of row k of W (the A4 operand) into 16 bytes of shared
+// memory: by cp.async from the fp16 copy or a kept row, or dequantized from the
+// codes.  The codes are requested here into registers (their loads stay in
+// flight while the weights stream) and converted by w8_finish before the
+// staged rows are read.  All sources are constant inputs.
+struct W8Pending {
+    int q[8];
+    __half* dst;  // nullptr: nothing pending
+    int nb;
+};
+
+__device__ __forceinline__ int ldg_nc_s8(const int8_t* p) {
+    int v;
+    asm volatile("ld.global.nc.s8 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void stage_w16_8(const GemvArgs& a, __half* dst, int k, int nb, W8Pending& pend) {
+    if (!a.w8) {
+        cp_async16(dst, a.W16 + (size_t)k * a.N + nb);
+        return;
+    }
+    const int rm = a.row_map != nullptr ? __ldg(a.row_map + k) : -1;
+    if (rm >= 0 && rm < a.w16_rows) {
+        cp_async16(dst, a.W16c + (size_t)rm * a.N + nb);
+        return;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) pend.q[e] = ldg_nc_s8(a.Wq + (size_t)(nb + e) * a.K + k);
+    pend.dst = dst;
+    pend.nb = nb;
+}
+
+__device__ __forceinline__ void w8_finish(const GemvArgs& a, W8Pending& pend) {
+    if (pend.dst == nullptr) return;
+    uint32_t h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __half lo = dequant_weight((int8_t)pend.q[2 * e], a.col_scale[pend.nb + 2 * e]);
+        const __half hi = dequant_weight((int8_t)pend.q[2 * e + 1], a.col_scale[pend.nb + 2 * e + 1]);
+        h[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+    }
+    *reinterpret_cast<uint4*>(pend.dst) = make_uint4(h[0], h[1], h[2], h[3]);
+    pend.dst = nullptr;
+}
+
+// One element of row k of W (the A4 operand) at column n, from the same sources.
+__device__ __forceinline__ float w16_value(const GemvArgs& a, int k, int n) {
+    if (!a.w8) return __half2float(a.W16[(size_t)k * a.N + n]);
+    const int rm = a.row_map != nullptr ? __ldg(a.row_map + k) : -1;
+    if (rm >= 0 && rm < a.w16_rows) return __half2float(a.W16c[(size_t)rm * a.N + n]);
+    return __half2float(dequant_weight(a.Wq[(size_t)n * a.K + k], a.col_scale[n]));
+}
 
 __device__ __forceinline__ void imma_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                            uint32_t b0, uint32_t b1) {
@@ -159,11 +220,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
     const int nidx = min(K, kGemvOutChunk);
     const int k_first = (outl && (tid >> 1) < nidx) ? ldg_cg_s32(a.outlier_idx + (tid >> 1)) : 0;
     const int cnt = outl ? ldg_cg_s32(&a.hdr->outlier_count) : 0;
+    W8Pending pend;
+    pend.dst = nullptr;
     auto stage_outliers = [&](int base, int c) {
         for (int e = tid; e < 2 * nidx; e += kGemvWarps * 32) {
             const int j = e >> 1, hv = e & 1;
             const int k = base == 0 ? k_first : (base + j < K ? __ldcg(a.outlier_idx + base + j) : 0);
-            if (j < c) cp_async16(&s_w16o[j][hv * 8], a.W16 + (size_t)k * a.N + n0 + hv * 8);
+            if (j < c) stage_w16_8(a, &s_w16o[j][hv * 8], k, n0 + hv * 8, pend);
         }
         const int cv = (c + 7) >> 3;
         for (int e = tid; e < a.M * (kGemvOutChunk / 8); e += kGemvWarps * 32) {
@@ -231,6 +294,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
     // No copy may still target shared memory: the ring is drained (its later
     // groups are empty) and the staging group has landed.  Each warp's partials
     // then go to its own ring, [16 x rows][16 columns] int32.
+    w8_finish(a, pend);
     cp_async_wait_all();
     int32_t* red = reinterpret_cast<int32_t*>(ring);
     // accumulator layout: d0,d1 -> (column g, x rows 8t+2q, +1); d2,d3 -> (column g+8, same rows)
@@ -264,6 +328,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
             if (base >= cnt) break;
             __syncthreads();
             stage_outliers(base, min(kGemvOutChunk, cnt - base));
+            w8_finish(a, pend);
             cp_async_wait_all();
             __syncthreads();
         }
@@ -386,10 +451,12 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode_tiles(GemvAr
         }
     }
     __syncthreads();  // s_idx
+    W8Pending pend;  // dequantized rows of the staged tile, converted before its epilogue
+    pend.dst = nullptr;
     auto stage_w16 = [&](int buf, int n0) {
         for (int e = tid; e < 2 * cst; e += kGemvWarps * 32) {
             const int jx = e >> 1, hv = e & 1;
-            cp_async16(&s_w16o[buf][jx][hv * 8], a.W16 + (size_t)s_idx[jx] * a.N + n0 + hv * 8);
+            stage_w16_8(a, &s_w16o[buf][jx][hv * 8], s_idx[jx], n0 + hv * 8, pend);
         }
         cp_async_commit();
     };
@@ -460,6 +527,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode_tiles(GemvAr
             cp_async_wait_group<R - 1>();
         else
             cp_async_wait_all();
+        w8_finish(a, pend);
         __syncthreads();  // partials and staged operands visible to all
         // the other staging buffer was last read by the previous tile's
         // epilogue, which every thread finished before the barrier ending it
@@ -480,7 +548,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode_tiles(GemvAr
             for (int jj = cst; jj < cnt; ++jj) {  // past the staged chunk: through L2
                 const int k = __ldcg(a.outlier_idx + jj);
                 const __half xv = __ldcg(a.xo + (size_t)ri * a.xo_pitch + jj);
-                f = fmaf(__half2float(xv), __half2float(a.W16[(size_t)k * a.N + n]), f);
+                f = fmaf(__half2float(xv), w16_value(a, k, n), f);
             }
             const float scale = rs * cs * (1.0f / 16129.0f);
             reinterpret_cast<__half*>(a.out)[(size_t)ri * a.N + n] = __float2half_rn(fmaf((float)c, scale, f));

@@ -93,4 +93,26 @@ __global__ void __launch_bounds__(256) k_quantize_weight_tile(const __half* __re
     }
 }
 
+// Kept fp16 rows of W (A4 without a full fp16 copy): row_map[k] = -1 for all k,
+// then for each listed row r: W16c[r, :] = W16[rows[r], :] and row_map[rows[r]] = r.
+// A listed row outside [0, K) gets a zero row and no map entry.
+__global__ void __launch_bounds__(256) k_row_map_clear(int32_t* __restrict__ row_map, int K) {
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += gridDim.x * blockDim.x) row_map[k] = -1;
+}
+
+__global__ void __launch_bounds__(256) k_pack_w16_rows(const __half* __restrict__ W16, int K, int N,
+                                                       const int32_t* __restrict__ rows, int nrows,
+                                                       __half* __restrict__ W16c, int32_t* __restrict__ row_map) {
+    const int vec = N / 8;  // 16-byte vectors per row
+    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < (size_t)nrows * vec;
+         e += (size_t)gridDim.x * blockDim.x) {
+        const int r = (int)(e / vec), v = (int)(e - (size_t)r * vec);
+        const int k = rows[r];
+        const bool ok = k >= 0 && k < K;
+        const uint4 val = ok ? ldg_nc_v4(W16 + (size_t)k * N + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(W16c + (size_t)r * N + 8 * v) = val;
+        if (ok && v == 0) row_map[k] = r;
+    }
+}
+
 }  // namespace llmint8

@@ -578,10 +578,22 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) k_row_quant_warp(RowQuantArg
 // for p < count, zero for count <= p < roundup(count, 64).  W16 is [K, N]
 // row-major; the result is [N, pitch] with the gathered K contiguous, the
 // K-major layout the MMA reads.  grid.x = ceil(N / 64); 256 threads.
+// W8Rows: the A4 operand when no full fp16 copy of W is kept (W16 is then
+// nullptr): row k is W16c[row_map[k]] if 0 <= row_map[k] < rows, else the
+// dequantized codes Wq[n, k] with colScaleW[n].
+struct W8Rows {
+    const __half* W16c;
+    const int32_t* row_map;
+    int rows;
+    const int8_t* Wq;  // [N, K]
+    int K;
+    const float* col_scale;
+};
+
 __global__ void __launch_bounds__(256) k_gather_w16_outlier_rows(const __half* __restrict__ W16, int N,
                                                                  const WsHeader* __restrict__ hdr,
                                                                  const int32_t* __restrict__ outlier_idx,
-                                                                 __half* __restrict__ w16oT, int pitch) {
+                                                                 __half* __restrict__ w16oT, int pitch, W8Rows w8) {
     __shared__ __half tile[64][64 + 8];
     pdl_trigger();
     pdl_wait();
@@ -595,7 +607,16 @@ __global__ void __launch_bounds__(256) k_gather_w16_outlier_rows(const __half* _
             const int pr = e >> 6, nc = e & 63;
             const int p = p0 + pr, n = n0 + nc;
             __half v = __ushort_as_half(0);
-            if (p < count && n < N) v = W16[(size_t)__ldcg(outlier_idx + p) * N + n];
+            if (p < count && n < N) {
+                const int k = __ldcg(outlier_idx + p);
+                if (W16 != nullptr) {
+                    v = W16[(size_t)k * N + n];
+                } else {
+                    const int rm = w8.row_map != nullptr ? __ldg(w8.row_map + k) : -1;
+                    v = (rm >= 0 && rm < w8.rows) ? w8.W16c[(size_t)rm * N + n]
+                                                  : dequant_weight(w8.Wq[(size_t)n * w8.K + k], w8.col_scale[n]);
+                }
+            }
             tile[pr][nc] = v;
         }
         __syncthreads();

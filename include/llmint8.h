@@ -107,6 +107,56 @@ llmint8_status llmint8_matmul(const void *X, int M, int K, int N, float threshol
                               void *stream);
 
 /*
+ * llmint8_matmul without a full fp16 copy of W (int8 weight storage only).  The
+ * outlier slice (A4) needs row k of W for every outlier column k of X: it is
+ * W16c[row_map[k], :] when 0 <= row_map[k] < w16_rows (rows the caller chose to
+ * keep in fp16, e.g. the columns that were outliers on calibration data), and
+ * otherwise the dequantized codes, w_hat[k, n] = fp16(fp32(Wq[n, k]) *
+ * fp32(colScaleW[n] / 127)) with each step rounded to nearest even.  The int8
+ * part (A3) and the merge (A5) are those of llmint8_matmul; with every row kept
+ * the result equals llmint8_matmul's.  Memory: w16_rows * N * 2 + K * 4 bytes
+ * instead of K * N * 2 for the fp16 copy.
+ *
+ *   W16c       in   fp16 [w16_rows, N] kept rows (from llmint8_pack_w16_rows);
+ *                   may be NULL when w16_rows = 0
+ *   row_map    in   int32 [K] device array, or NULL when no row is kept
+ *   w16_rows   in   number of kept rows (>= 0); map entries >= w16_rows count as
+ *                   not kept
+ *   other arguments as llmint8_matmul (without W16)
+ *
+ * Errors as llmint8_matmul; EINVAL also for w16_rows < 0, or w16_rows > 0 with a
+ * NULL W16c or row_map; EALIGN for a W16c that is not 16-byte aligned.
+ * Source: paper walkthrough, section 2.3 (the outlier slice in fp16); pitfalls
+ * guide, section 1 (codes dequantized by their scale); Lightning Fabric 8-bit
+ * page, section 2.2 (one scale per output column).
+ */
+llmint8_status llmint8_matmul_w8(const void *X, int M, int K, int N, float threshold,
+                                 const int8_t *Wq, const float *colScaleW, const void *Wq16,
+                                 const void *W16c, const int32_t *row_map, int w16_rows, void *Y,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Builds the kept rows for llmint8_matmul_w8 from a full fp16 W [K, N] (once, at
+ * load time; the full copy can be freed afterwards): row_map[k] = -1 for every
+ * k, then for each r < w16_rows, W16c[r, :] = W16[rows[r], :] and
+ * row_map[rows[r]] = r.  A listed row outside [0, K) gets a zero row in W16c and
+ * no map entry.
+ *
+ *   W16        in   fp16 [K, N] device
+ *   rows       in   int32 [w16_rows] device, the rows to keep (may be NULL when
+ *                   w16_rows = 0)
+ *   W16c       out  fp16 [w16_rows, N] device (may be NULL when w16_rows = 0)
+ *   row_map    out  int32 [K] device
+ *
+ * Errors: EINVAL for a NULL W16 or row_map, K or N <= 0, K > 65536, w16_rows < 0,
+ * or w16_rows > 0 with a NULL rows or W16c; EALIGN if N is not a multiple of 16
+ * or W16 or W16c is not 16-byte aligned; ECUDA if a launch fails.  Asynchronous
+ * on `stream`.
+ */
+llmint8_status llmint8_pack_w16_rows(const void *W16, int K, int N, const int32_t *rows, int w16_rows,
+                                     void *W16c, int32_t *row_map, void *stream);
+
+/*
  * Plain vector-wise int8 variant: llmint8_matmul with threshold = +INFINITY and
  * no fp16 weight.  Row scales run over all K columns; Y = fp16(C * sx * sw / 127^2).
  * Source: pitfalls guide, section 1 (plain absmax int8, no outlier handling).

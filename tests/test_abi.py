@@ -143,3 +143,17 @@ def test_kernels_per_call(lib):
     assert k(17, 4096, 4096, inf, 0) == 2
     assert k(0, 64, 64, 6.0, 0) == -1
     assert k(1, 64, 64, math.nan, 0) == -1
+
+
+def test_w8_argument_errors(lib):
+    from bit_quantization_matmul_row_b300 import _lib
+    P = ctypes.c_void_p
+    ws = lib.llmint8_workspace_bytes(16, 64, 64)
+    args = lambda W16c, rmap, rows: (P(FAKE), 16, 64, 64, 6.0, P(FAKE), P(FAKE), P(FAKE), W16c, rmap, rows,
+                                     P(FAKE), P(FAKE), ws, None)
+    assert lib.llmint8_matmul_w8(*args(None, None, -1)) == _lib.EINVAL
+    assert lib.llmint8_matmul_w8(*args(None, P(FAKE), 4)) == _lib.EINVAL   # rows kept, no W16c
+    assert lib.llmint8_matmul_w8(*args(P(FAKE + 4), P(FAKE), 4)) == _lib.EALIGN
+    assert lib.llmint8_pack_w16_rows(None, 64, 64, None, 0, None, P(FAKE), None) == _lib.EINVAL
+    assert lib.llmint8_pack_w16_rows(P(FAKE), 64, 64, None, 3, P(FAKE), P(FAKE), None) == _lib.EINVAL
+    assert lib.llmint8_pack_w16_rows(P(FAKE), 64, 40, None, 0, None, P(FAKE), None) == _lib.EALIGN
