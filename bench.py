@@ -530,7 +530,8 @@ def run_prefill(args, dev, stream, bf16_peak, peak_src, iters=None):
 
 
 def run_ablation(args):
-    """Error vs speed of the LLM.int8() decomposition against plain vector-wise int8
+    """Error vs speed of the LLM.int8() decomposition (with the fp16 copy of W, and
+    with int8 weights only) against plain vector-wise int8
     (threshold +inf: no outlier decomposition) and the fp16 matmul (cuBLAS, context),
     on the synthetic outlier workloads.  Error: relative Frobenius distance to the
     exact product (fp64 on the GPU).  Times: CUDA events around single calls."""
@@ -556,6 +557,8 @@ def run_ablation(args):
         exact = Xd.double() @ Wd.double()
         variants = {
             "llmint8_t6": lambda r: api.llmint8_matmul(Xd, 6.0, r[0], r[1], r[2], r[3], workspace=ws),
+            # no fp16 copy of W kept: the outlier rows come from the dequantized codes
+            "llmint8_t6_int8_weights": lambda r: api.llmint8_matmul_w8(Xd, 6.0, r[0], r[1], r[2], workspace=ws),
             "int8_no_outliers": lambda r: api.llmint8_matmul_int8(Xd, r[0], r[1], r[2], workspace=ws),
             "fp16_cublas": lambda r: torch.matmul(Xd, r[3]),
         }
