@@ -41,13 +41,34 @@ def planted_count(K: int, frac: float, min_count: int = 0) -> int:
     return min(n, K)
 
 
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), rounded to nearest even.
+
+    The input generators' bf16 cast (numpy has no bfloat16 type): the upper 16
+    bits of the binary32 value after adding 0x7fff plus the lowest kept bit.
+    Inputs here are finite.
+    """
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def _cast(x: np.ndarray, fmt: str) -> np.ndarray:
+    if fmt == "fp16":
+        return x.astype(np.float16)
+    if fmt == "bf16":
+        return to_bf16_bits(x)
+    raise ValueError(fmt)
+
+
 def make_x(M: int, K: int, *, frac: float = 0.0, min_count: int = 0,
-           mag: tuple[float, float] = (20.0, 60.0), seed: int = 0):
+           mag: tuple[float, float] = (20.0, 60.0), seed: int = 0, fmt: str = "fp16"):
     """X fp16 [M, K] ~ N(0,1) with planted outlier columns.
 
     Returns (X, planted) where planted is the sorted int64 array of the
     planted column indices.  Column j in `planted` is rescaled so that
-    max_i |X[i, j]| == U(mag) (before the fp16 cast).
+    max_i |X[i, j]| == U(mag) (before the cast).  fmt="bf16" returns X as
+    bfloat16 bit patterns (uint16) of the same draws.
     """
     g = _rng(seed, X_STREAM)
     x = g.standard_normal((M, K), dtype=np.float32)
@@ -59,11 +80,11 @@ def make_x(M: int, K: int, *, frac: float = 0.0, min_count: int = 0,
         peak = np.max(np.abs(sub), axis=0)
         peak[peak == 0] = 1.0
         x[:, cols] = sub * (target / peak)[None, :]
-    return x.astype(np.float16), cols.astype(np.int64)
+    return _cast(x, fmt), cols.astype(np.int64)
 
 
 def make_w(K: int, N: int, *, sigma: float = 0.02, boosted_frac: float = 0.0,
-           boost: float = 10.0, seed: int = 0):
+           boost: float = 10.0, seed: int = 0, fmt: str = "fp16"):
     """W fp16 [K, N] ~ N(0, sigma); a fraction of the N-columns is multiplied by `boost`.
 
     Returns (W, boosted) with boosted the sorted column indices that were scaled.
@@ -74,7 +95,7 @@ def make_w(K: int, N: int, *, sigma: float = 0.02, boosted_frac: float = 0.0,
     cols = np.sort(g.choice(N, size=nb, replace=False)) if nb else np.zeros(0, np.int64)
     if nb:
         w[:, cols] *= np.float32(boost)
-    return w.astype(np.float16), cols.astype(np.int64)
+    return _cast(w, fmt), cols.astype(np.int64)
 
 
 @dataclass(frozen=True)

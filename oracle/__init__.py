@@ -68,8 +68,21 @@ def _load():
             lib.oracle_outlier_matmul.argtypes = [P, P, P, I, I, I, P, ctypes.c_int]
             lib.oracle_merge.argtypes = [P, P, P, P, I, I, P]
             lib.oracle_dequantize_weight.argtypes = [P, P, I, I, P]
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = ctypes.c_double
+            lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+            C = ctypes.c_int
+            lib.oracle_quantize_weight_fmt.argtypes = [P, I, I, P, P, C]
+            lib.oracle_outlier_columns_fmt.argtypes = [P, I, I, ctypes.c_float, P, C]
+            lib.oracle_quantize_rows_fmt.argtypes = [P, I, I, P, P, P, C]
+            lib.oracle_outlier_matmul_fmt.argtypes = [P, P, P, I, I, I, P, C, C]
+            lib.oracle_merge_fmt.argtypes = [P, P, P, P, I, I, P, C]
+            lib.oracle_dequantize_weight_fmt.argtypes = [P, P, I, I, P, C]
             for f in ("oracle_quantize_weight", "oracle_outlier_columns", "oracle_quantize_rows",
                       "oracle_quantize_per_tensor", "oracle_dequantize_weight",
+                      "oracle_quantize_weight_fmt", "oracle_outlier_columns_fmt", "oracle_quantize_rows_fmt",
+                      "oracle_outlier_matmul_fmt", "oracle_merge_fmt", "oracle_dequantize_weight_fmt",
                       "oracle_int8_matmul", "oracle_outlier_matmul", "oracle_merge"):
                 getattr(lib, f).restype = None
             _lib = lib
@@ -81,13 +94,22 @@ def _ptr(a: np.ndarray):
 
 
 def _bits(a) -> np.ndarray:
-    """fp16 array -> contiguous uint16 bit pattern."""
+    """fp16 array (or uint16 bit patterns: fp16, or bf16 data) -> contiguous uint16."""
     a = np.ascontiguousarray(a)
     if a.dtype == np.float16:
         return a.view(np.uint16)
     if a.dtype == np.uint16:
         return a
-    raise TypeError(f"expected float16 data, got {a.dtype}")
+    raise TypeError(f"expected float16 data or uint16 bit patterns, got {a.dtype}")
+
+
+# 16-bit element formats of X, W and Y: fp16 (numpy float16 or its bits) or
+# bf16 (uint16 bit patterns; numpy has no bfloat16)
+_FMT = {"fp16": 0, "bf16": 1}
+
+
+def _out16(bits: np.ndarray, fmt: str) -> np.ndarray:
+    return bits.view(np.float16) if fmt == "fp16" else bits
 
 
 def default_threads() -> int:
@@ -108,6 +130,14 @@ def scale_factor(absmax: float) -> float:
     return float(_load().oracle_scale_factor(float(absmax)))
 
 
+def bf16_to_double(bits: int) -> float:
+    return _load().oracle_bf16_to_double(int(bits))
+
+
+def double_to_bf16(v: float) -> int:
+    return _load().oracle_double_to_bf16(float(v))
+
+
 def code(x: float, sf: float) -> int:
     return int(_load().oracle_code(float(x), float(sf)))
 
@@ -122,33 +152,33 @@ def to_half(values: np.ndarray) -> np.ndarray:
 
 # -- method steps -------------------------------------------------------------------
 
-def quantize_weight(W: np.ndarray):
-    """A0: W fp16 [K,N] -> (Wq int8 [K,N], s_w float32 [N] = column absmax)."""
+def quantize_weight(W: np.ndarray, fmt: str = "fp16"):
+    """A0: W [K,N] -> (Wq int8 [K,N], s_w float32 [N] = column absmax)."""
     Wb = _bits(W)
     K, N = Wb.shape
     Wq = np.empty((K, N), np.int8)
     sw = np.empty(N, np.float32)
-    _load().oracle_quantize_weight(_ptr(Wb), K, N, _ptr(Wq), _ptr(sw))
+    _load().oracle_quantize_weight_fmt(_ptr(Wb), K, N, _ptr(Wq), _ptr(sw), _FMT[fmt])
     return Wq, sw
 
 
-def outlier_columns(X: np.ndarray, t: float) -> np.ndarray:
+def outlier_columns(X: np.ndarray, t: float, fmt: str = "fp16") -> np.ndarray:
     """A1: bool [K], True where some |X[i,j]| > t."""
     Xb = _bits(X)
     M, K = Xb.shape
     out = np.empty(K, np.uint8)
-    _load().oracle_outlier_columns(_ptr(Xb), M, K, float(t), _ptr(out))
+    _load().oracle_outlier_columns_fmt(_ptr(Xb), M, K, float(t), _ptr(out), _FMT[fmt])
     return out.astype(bool)
 
 
-def quantize_rows(X: np.ndarray, is_outlier: np.ndarray):
+def quantize_rows(X: np.ndarray, is_outlier: np.ndarray, fmt: str = "fp16"):
     """A2: (Xq int8 [M,K] with outlier columns zero, s_x float32 [M])."""
     Xb = _bits(X)
     M, K = Xb.shape
     mask = np.ascontiguousarray(is_outlier, dtype=np.uint8)
     Xq = np.empty((M, K), np.int8)
     sx = np.empty(M, np.float32)
-    _load().oracle_quantize_rows(_ptr(Xb), M, K, _ptr(mask), _ptr(Xq), _ptr(sx))
+    _load().oracle_quantize_rows_fmt(_ptr(Xb), M, K, _ptr(mask), _ptr(Xq), _ptr(sx), _FMT[fmt])
     return Xq, sx
 
 
@@ -165,7 +195,7 @@ def int8_matmul(Xq: np.ndarray, Wq: np.ndarray, nthreads: int | None = None) -> 
 
 
 def outlier_matmul(X: np.ndarray, W: np.ndarray, is_outlier: np.ndarray,
-                   nthreads: int | None = None) -> np.ndarray:
+                   nthreads: int | None = None, fmt: str = "fp16") -> np.ndarray:
     """A4: F = X[:, O] . W[O, :] in double."""
     Xb, Wb = _bits(X), _bits(W)
     M, K = Xb.shape
@@ -173,13 +203,13 @@ def outlier_matmul(X: np.ndarray, W: np.ndarray, is_outlier: np.ndarray,
     assert K == K2
     mask = np.ascontiguousarray(is_outlier, dtype=np.uint8)
     F = np.empty((M, N), np.float64)
-    _load().oracle_outlier_matmul(_ptr(Xb), _ptr(Wb), _ptr(mask), M, K, N, _ptr(F),
-                                  nthreads or default_threads())
+    _load().oracle_outlier_matmul_fmt(_ptr(Xb), _ptr(Wb), _ptr(mask), M, K, N, _ptr(F),
+                                      nthreads or default_threads(), _FMT[fmt])
     return F
 
 
-def merge(C: np.ndarray, s_x: np.ndarray, s_w: np.ndarray, F: np.ndarray | None) -> np.ndarray:
-    """A5: Y fp16 = RNE(C * s_x * s_w / 127^2 + F)."""
+def merge(C: np.ndarray, s_x: np.ndarray, s_w: np.ndarray, F: np.ndarray | None, fmt: str = "fp16") -> np.ndarray:
+    """A5: Y = RNE(C * s_x * s_w / 127^2 + F) in the output format (fp16, or bf16 bits)."""
     C = np.ascontiguousarray(C, np.int64)
     M, N = C.shape
     sx = np.ascontiguousarray(s_x, np.float32)
@@ -189,8 +219,8 @@ def merge(C: np.ndarray, s_x: np.ndarray, s_w: np.ndarray, F: np.ndarray | None)
         F = np.ascontiguousarray(F, np.float64)
         Fp = _ptr(F)
     Y = np.empty((M, N), np.uint16)
-    _load().oracle_merge(_ptr(C), _ptr(sx), _ptr(sw), Fp, M, N, _ptr(Y))
-    return Y.view(np.float16)
+    _load().oracle_merge_fmt(_ptr(C), _ptr(sx), _ptr(sw), Fp, M, N, _ptr(Y), _FMT[fmt])
+    return _out16(Y, fmt)
 
 
 def quantize_per_tensor(A: np.ndarray):
@@ -211,14 +241,14 @@ def per_tensor_int8_matmul(X: np.ndarray, W: np.ndarray, nthreads: int | None = 
     return merge(C, np.full(M, sx, np.float32), np.full(N, sw, np.float32), None)
 
 
-def dequantize_weight(Wq: np.ndarray, s_w: np.ndarray) -> np.ndarray:
-    """A4 weight rows when only the int8 codes are kept: fp16(q * (s_w / 127)) [K,N]."""
+def dequantize_weight(Wq: np.ndarray, s_w: np.ndarray, fmt: str = "fp16") -> np.ndarray:
+    """A4 weight rows when only the int8 codes are kept: RNE(q * (s_w / 127)) [K,N] in fmt."""
     Wq = np.ascontiguousarray(Wq, np.int8)
     K, N = Wq.shape
     sw = np.ascontiguousarray(s_w, np.float32)
     out = np.empty((K, N), np.uint16)
-    _load().oracle_dequantize_weight(_ptr(Wq), _ptr(sw), K, N, _ptr(out))
-    return out.view(np.float16)
+    _load().oracle_dequantize_weight_fmt(_ptr(Wq), _ptr(sw), K, N, _ptr(out), _FMT[fmt])
+    return _out16(out, fmt)
 
 
 def outlier_indices(is_outlier: np.ndarray) -> np.ndarray:
@@ -227,7 +257,7 @@ def outlier_indices(is_outlier: np.ndarray) -> np.ndarray:
 
 
 def llmint8_matmul(X: np.ndarray, W: np.ndarray, t: float, rows=None, nthreads: int | None = None,
-                   wq=None, cols=None, w16_rows=None):
+                   wq=None, cols=None, w16_rows=None, fmt: str = "fp16"):
     """The whole path A0..A5 for Y = X.W with threshold t.
 
     Outlier detection (A1) always scans all rows of X, because the outlier set
@@ -238,22 +268,23 @@ def llmint8_matmul(X: np.ndarray, W: np.ndarray, t: float, rows=None, nthreads: 
     runs on W[:, cols].  ``wq`` may pass a precomputed (Wq, s_w) from
     quantize_weight of the (restricted) W.  ``w16_rows`` (optional index
     array) selects the mode where only those rows of W are kept in fp16: A4
-    then takes every other outlier row from dequantize_weight.  Returns a dict
-    with every intermediate.
+    then takes every other outlier row from dequantize_weight.  ``fmt="bf16"``
+    takes X and W as bfloat16 bit patterns (uint16) and returns Y in bfloat16
+    bits.  Returns a dict with every intermediate.
     """
     if cols is not None:
         W = np.ascontiguousarray(W[:, np.asarray(cols)])
-    Wq, s_w = wq if wq is not None else quantize_weight(W)
-    is_out = outlier_columns(X, t)
+    Wq, s_w = wq if wq is not None else quantize_weight(W, fmt)
+    is_out = outlier_columns(X, t, fmt)
     Xs = X if rows is None else np.ascontiguousarray(X[np.asarray(rows)])
-    Xq, s_x = quantize_rows(Xs, is_out)
+    Xq, s_x = quantize_rows(Xs, is_out, fmt)
     C = int8_matmul(Xq, Wq, nthreads)
     W4 = W
     if w16_rows is not None:  # fp16 rows only where kept, dequantized codes elsewhere
         keep = np.zeros(W.shape[0], bool)
         keep[np.asarray(w16_rows, np.int64)] = True
-        W4 = np.where(keep[:, None], W, dequantize_weight(Wq, s_w))
-    F = outlier_matmul(Xs, W4, is_out, nthreads) if is_out.any() else np.zeros(C.shape, np.float64)
-    Y = merge(C, s_x, s_w, F)
+        W4 = np.where(keep[:, None], W, dequantize_weight(Wq, s_w, fmt))
+    F = outlier_matmul(Xs, W4, is_out, nthreads, fmt) if is_out.any() else np.zeros(C.shape, np.float64)
+    Y = merge(C, s_x, s_w, F, fmt)
     return dict(Y=Y, C=C, F=F, Xq=Xq, s_x=s_x, Wq=Wq, s_w=s_w, is_outlier=is_out,
                 outliers=outlier_indices(is_out))

@@ -26,6 +26,7 @@
  *
  * Layouts (all row-major, caller-owned host memory):
  *   X   fp16 bits [M,K]     W   fp16 bits [K,N]     Y fp16 bits [M,N]
+ *   (the *_fmt entry points take fmt = 1 for bfloat16 X, W and Y instead)
  *   Xq  int8 [M,K]          Wq  int8 [K,N]          C int64 [M,N]
  *   s_x float [M]           s_w float [N]           F double [M,N]
  *   is_outlier uint8 [K] (1 = column of X is an outlier dimension)
@@ -81,6 +82,62 @@ uint16_t oracle_double_to_half(double v)
     return sign | (uint16_t)((e + 15) << 10) | (uint16_t)((int)r - 1024);
 }
 
+/* ---------------------------------------------------------------------------
+ * bfloat16 <-> double, written from the format definition (1 sign bit, 8
+ * exponent bits with bias 127, 7 fraction bits: the upper half of a binary32).
+ * ------------------------------------------------------------------------- */
+double oracle_bf16_to_double(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133); /* subnormal: f * 2^-133 */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + f), e - 134); /* (1.f) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* Round-to-nearest-even conversion of a double to bfloat16 (overflow -> inf). */
+uint16_t oracle_double_to_bf16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isnan(v))
+        return 0x7fc0;
+    /* halfway between the largest finite value (2 - 2^-7) * 2^127 and 2^128 */
+    if (a >= ldexp(2.0 - ldexp(1.0, -8), 127))
+        return sign | 0x7f80;
+    if (a < ldexp(1.0, -126)) {
+        /* subnormal range: value = q * 2^-133, q rounded to nearest even;
+         * q == 128 encodes the smallest normal number, which is correct. */
+        double q = nearbyint(ldexp(a, 133));
+        return sign | (uint16_t)q;
+    }
+    int e;
+    double m = frexp(a, &e);           /* a = m * 2^e, m in [0.5, 1) */
+    double r = nearbyint(ldexp(m, 8)); /* 8 significant bits, RNE */
+    e -= 1;                            /* a = (r/128) * 2^e */
+    if (r == 256.0) {
+        r = 128.0;
+        e += 1;
+    }
+    return sign | (uint16_t)((e + 127) << 7) | (uint16_t)((int)r - 128);
+}
+
+/* 16-bit floating-point element formats of X, W and Y: 0 = fp16, 1 = bf16. */
+static double elem_to_double(uint16_t v, int fmt)
+{
+    return fmt ? oracle_bf16_to_double(v) : oracle_half_to_double(v);
+}
+static uint16_t double_to_elem(double v, int fmt)
+{
+    return fmt ? oracle_double_to_bf16(v) : oracle_double_to_half(v);
+}
+static float elem_to_float(uint16_t v, int fmt) { return (float)elem_to_double(v, fmt); }
 static float half_to_float(uint16_t h) { return (float)oracle_half_to_double(h); }
 
 /* ---------------------------------------------------------------------------
@@ -114,20 +171,25 @@ int8_t oracle_code(float x, float scale_factor)
  * neuron).  The column absmax runs over all K rows, because W is quantized
  * once, before any X is seen.
  * ------------------------------------------------------------------------- */
-void oracle_quantize_weight(const uint16_t *W, int64_t K, int64_t N, int8_t *Wq, float *s_w)
+void oracle_quantize_weight_fmt(const uint16_t *W, int64_t K, int64_t N, int8_t *Wq, float *s_w, int fmt)
 {
     for (int64_t n = 0; n < N; ++n) {
         float amax = 0.0f;
         for (int64_t k = 0; k < K; ++k) {
-            float a = fabsf(half_to_float(W[k * N + n]));
+            float a = fabsf(elem_to_float(W[k * N + n], fmt));
             if (a > amax)
                 amax = a;
         }
         s_w[n] = amax;
         float sf = oracle_scale_factor(amax);
         for (int64_t k = 0; k < K; ++k)
-            Wq[k * N + n] = oracle_code(half_to_float(W[k * N + n]), sf);
+            Wq[k * N + n] = oracle_code(elem_to_float(W[k * N + n], fmt), sf);
     }
+}
+
+void oracle_quantize_weight(const uint16_t *W, int64_t K, int64_t N, int8_t *Wq, float *s_w)
+{
+    oracle_quantize_weight_fmt(W, K, N, Wq, s_w, 0);
 }
 
 /* ---------------------------------------------------------------------------
@@ -154,15 +216,20 @@ void oracle_quantize_per_tensor(const uint16_t *A, int64_t n, int8_t *q, float *
  * magnitude exceeds the threshold t (default 6.0) is an outlier column.
  * "Exceeds" is read as strict: |x| > t.
  * ------------------------------------------------------------------------- */
-void oracle_outlier_columns(const uint16_t *X, int64_t M, int64_t K, float t, uint8_t *is_outlier)
+void oracle_outlier_columns_fmt(const uint16_t *X, int64_t M, int64_t K, float t, uint8_t *is_outlier, int fmt)
 {
     for (int64_t j = 0; j < K; ++j) {
         int out = 0;
         for (int64_t i = 0; i < M; ++i)
-            if (fabsf(half_to_float(X[i * K + j])) > t)
+            if (fabsf(elem_to_float(X[i * K + j], fmt)) > t)
                 out = 1;
         is_outlier[j] = (uint8_t)out;
     }
+}
+
+void oracle_outlier_columns(const uint16_t *X, int64_t M, int64_t K, float t, uint8_t *is_outlier)
+{
+    oracle_outlier_columns_fmt(X, M, K, t, is_outlier, 0);
 }
 
 /* ---------------------------------------------------------------------------
@@ -172,23 +239,29 @@ void oracle_outlier_columns(const uint16_t *X, int64_t M, int64_t K, float t, ui
  * non-outlier columns; outlier columns get code 0 (they are carried by the
  * fp16 product instead).
  * ------------------------------------------------------------------------- */
-void oracle_quantize_rows(const uint16_t *X, int64_t M, int64_t K, const uint8_t *is_outlier,
-                          int8_t *Xq, float *s_x)
+void oracle_quantize_rows_fmt(const uint16_t *X, int64_t M, int64_t K, const uint8_t *is_outlier,
+                              int8_t *Xq, float *s_x, int fmt)
 {
     for (int64_t i = 0; i < M; ++i) {
         float amax = 0.0f;
         for (int64_t j = 0; j < K; ++j) {
             if (is_outlier[j])
                 continue;
-            float a = fabsf(half_to_float(X[i * K + j]));
+            float a = fabsf(elem_to_float(X[i * K + j], fmt));
             if (a > amax)
                 amax = a;
         }
         s_x[i] = amax;
         float sf = oracle_scale_factor(amax);
         for (int64_t j = 0; j < K; ++j)
-            Xq[i * K + j] = is_outlier[j] ? 0 : oracle_code(half_to_float(X[i * K + j]), sf);
+            Xq[i * K + j] = is_outlier[j] ? 0 : oracle_code(elem_to_float(X[i * K + j], fmt), sf);
     }
+}
+
+void oracle_quantize_rows(const uint16_t *X, int64_t M, int64_t K, const uint8_t *is_outlier,
+                          int8_t *Xq, float *s_x)
+{
+    oracle_quantize_rows_fmt(X, M, K, is_outlier, Xq, s_x, 0);
 }
 
 /* ---------------------------------------------------------------------------
@@ -284,6 +357,7 @@ typedef struct {
     const uint8_t *is_outlier;
     int64_t K, N;
     double *F;
+    int fmt;
 } omm_ctx;
 
 static void omm_rows(void *p, int64_t r0, int64_t r1)
@@ -294,17 +368,23 @@ static void omm_rows(void *p, int64_t r0, int64_t r1)
             double acc = 0.0;
             for (int64_t k = 0; k < c->K; ++k)
                 if (c->is_outlier[k])
-                    acc += oracle_half_to_double(c->X[i * c->K + k]) *
-                           oracle_half_to_double(c->W[k * c->N + n]);
+                    acc += elem_to_double(c->X[i * c->K + k], c->fmt) *
+                           elem_to_double(c->W[k * c->N + n], c->fmt);
             c->F[i * c->N + n] = acc;
         }
+}
+
+void oracle_outlier_matmul_fmt(const uint16_t *X, const uint16_t *W, const uint8_t *is_outlier,
+                               int64_t M, int64_t K, int64_t N, double *F, int nthreads, int fmt)
+{
+    omm_ctx c = {X, W, is_outlier, K, N, F, fmt};
+    for_rows(omm_rows, &c, M, nthreads);
 }
 
 void oracle_outlier_matmul(const uint16_t *X, const uint16_t *W, const uint8_t *is_outlier,
                            int64_t M, int64_t K, int64_t N, double *F, int nthreads)
 {
-    omm_ctx c = {X, W, is_outlier, K, N, F};
-    for_rows(omm_rows, &c, M, nthreads);
+    oracle_outlier_matmul_fmt(X, W, is_outlier, M, K, N, F, nthreads, 0);
 }
 
 /* ---------------------------------------------------------------------------
@@ -317,15 +397,21 @@ void oracle_outlier_matmul(const uint16_t *X, const uint16_t *W, const uint8_t *
  * each fp32 operation rounded once to nearest even, then rounded to fp16 (the
  * operand precision of the outlier product).  s_w = 0 gives 0.
  * ------------------------------------------------------------------------- */
-void oracle_dequantize_weight(const int8_t *Wq, const float *s_w, int64_t K, int64_t N, uint16_t *W_hat)
+void oracle_dequantize_weight_fmt(const int8_t *Wq, const float *s_w, int64_t K, int64_t N, uint16_t *W_hat,
+                                  int fmt)
 {
     for (int64_t n = 0; n < N; ++n) {
         float r = s_w[n] / 127.0f;
         for (int64_t k = 0; k < K; ++k) {
             float p = (float)Wq[k * N + n] * r;
-            W_hat[k * N + n] = oracle_double_to_half((double)p);
+            W_hat[k * N + n] = double_to_elem((double)p, fmt);
         }
     }
+}
+
+void oracle_dequantize_weight(const int8_t *Wq, const float *s_w, int64_t K, int64_t N, uint16_t *W_hat)
+{
+    oracle_dequantize_weight_fmt(Wq, s_w, K, N, W_hat, 0);
 }
 
 /* ---------------------------------------------------------------------------
@@ -335,13 +421,19 @@ void oracle_dequantize_weight(const int8_t *Wq, const float *s_w, int64_t K, int
  * carries a factor absmax/127, so the integer result is scaled by
  * s_x[i] * s_w[n] / 127^2.  Done in double, then rounded to fp16 (RNE).
  * ------------------------------------------------------------------------- */
-void oracle_merge(const int64_t *C, const float *s_x, const float *s_w, const double *F,
-                  int64_t M, int64_t N, uint16_t *Y)
+void oracle_merge_fmt(const int64_t *C, const float *s_x, const float *s_w, const double *F,
+                      int64_t M, int64_t N, uint16_t *Y, int fmt)
 {
     for (int64_t i = 0; i < M; ++i)
         for (int64_t n = 0; n < N; ++n) {
             double deq = (double)C[i * N + n] * (double)s_x[i] * (double)s_w[n] / 16129.0;
             double y = deq + (F ? F[i * N + n] : 0.0);
-            Y[i * N + n] = oracle_double_to_half(y);
+            Y[i * N + n] = double_to_elem(y, fmt);
         }
+}
+
+void oracle_merge(const int64_t *C, const float *s_x, const float *s_w, const double *F,
+                  int64_t M, int64_t N, uint16_t *Y)
+{
+    oracle_merge_fmt(C, s_x, s_w, F, M, N, Y, 0);
 }

@@ -404,3 +404,98 @@ def test_all_rows_kept_in_fp16_is_the_standard_path(oracle_mod):
     a = oracle_mod.llmint8_matmul(X, W, math.inf)
     b = oracle_mod.llmint8_matmul(X, W, math.inf, w16_rows=np.array([], np.int64))
     assert np.array_equal(a["Y"].view(np.uint16), b["Y"].view(np.uint16))
+
+
+# ---------------------------------------------------------------------------------
+# bfloat16 inputs and output (the same method on bf16 X, W, Y)
+# ---------------------------------------------------------------------------------
+
+def _bf16_values(bits):
+    """bf16 bit patterns -> float64 values through torch (an independent library)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).astype(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def bf16_ulp(y):
+    a = np.abs(np.asarray(y, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def test_bf16_to_double_all_bit_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = _bf16_values(bits)
+    got = np.array([oracle_mod.bf16_to_double(int(b)) for b in bits])
+    finite = ~np.isnan(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.all(np.isnan(got[~finite]))
+
+
+def test_double_to_bf16_matches_torch(oracle_mod):
+    import torch
+    rng = np.random.default_rng(3)
+    v = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-30, 30, 20000),
+        # exact midpoints between neighbouring bf16 values (ties to even)
+        (_bf16_values(np.arange(0, 30000, 7, dtype=np.uint16)) * (1 + 2.0 ** -8)).astype(np.float32),
+        np.array([3.3895314e38, 3.4e38, 1e-40, 9.2e-41, -0.0, 0.0], np.float32),
+    ]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle_mod.double_to_bf16(float(x)) for x in v], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_worked_example_in_bf16(oracle_mod):
+    # The pitfalls guide's four values rounded to bf16 still give its codes, its
+    # scale and its printed dequantized values.
+    g = _read_golden("worked_example.txt")
+    bits = synthetic.to_bf16_bits(np.array(g["values"], np.float32)).reshape(4, 1)
+    Wq, sw = oracle_mod.quantize_weight(bits, "bf16")
+    assert Wq[:, 0].tolist() == [int(c) for c in g["codes"]]
+    assert sw[0] == 12.0
+    deq = oracle_mod.dequantize_weight(Wq, sw, "bf16")[:, 0]
+    assert [round(float(v), 2) for v in _bf16_values(deq)] == g["dequantized_2dp"]
+
+
+def test_bf16_threshold_zero_is_the_bf16_matmul(oracle_mod):
+    X, _ = synthetic.make_x(12, 96, seed=21, fmt="bf16")
+    X[:, 5] = 0
+    W, _ = synthetic.make_w(96, 40, seed=21, fmt="bf16")
+    r = oracle_mod.llmint8_matmul(X, W, 0.0, fmt="bf16")
+    assert r["outliers"].size == 95 and not r["C"].any()
+    ref = _bf16_values(X) @ _bf16_values(W)
+    diff = np.abs(_bf16_values(r["Y"]) - ref)
+    assert np.all(diff <= bf16_ulp(ref) / 2 + 1e-30)
+
+
+@pytest.mark.parametrize("t", [math.inf, 6.0])
+def test_bf16_quantization_error_bound(oracle_mod, t):
+    # the fp16 bound of test_quantization_error_bound, with a bf16 final rounding
+    X, _ = synthetic.make_x(24, 200, frac=0.02, seed=22, fmt="bf16")
+    W, _ = synthetic.make_w(200, 72, seed=22, fmt="bf16")
+    r = oracle_mod.llmint8_matmul(X, W, t, fmt="bf16")
+    keep = ~r["is_outlier"]
+    Xd, Wd = _bf16_values(X), _bf16_values(W)
+    xhat = r["Xq"].astype(np.float64) * r["s_x"][:, None].astype(np.float64) / 127
+    sx = r["s_x"].astype(np.float64)[:, None]
+    sw = r["s_w"].astype(np.float64)[None, :]
+    slack = 1 / 254 + 1e-6
+    bound = (sx * slack) * np.abs(Wd[keep]).sum(0)[None, :] + (np.abs(xhat[:, keep]).sum(1)[:, None]) * sw * slack
+    ref = Xd @ Wd
+    err = np.abs(_bf16_values(r["Y"]) - ref)
+    assert np.all(err <= bound + bf16_ulp(ref) + 1e-12)
+    assert np.max(err) < 0.05 * np.max(np.abs(ref))
+
+
+def test_bf16_and_fp16_agree_on_values_both_represent(oracle_mod):
+    # Inputs with at most 8 significant bits inside fp16's normal range are the
+    # same numbers in both formats: codes, scales, outlier set and C coincide.
+    rng = np.random.default_rng(23)
+    Xv = (rng.integers(-255, 256, (10, 128)) / 32.0).astype(np.float32)
+    Xv[:, [4, 77]] *= 8
+    Wv = (rng.integers(-127, 128, (128, 48)) / 4096.0).astype(np.float32)
+    a = oracle_mod.llmint8_matmul(Xv.astype(np.float16), Wv.astype(np.float16), 6.0)
+    b = oracle_mod.llmint8_matmul(synthetic.to_bf16_bits(Xv), synthetic.to_bf16_bits(Wv), 6.0, fmt="bf16")
+    for k in ("Xq", "s_x", "Wq", "s_w", "C", "outliers", "F"):
+        assert np.array_equal(a[k], b[k]), k
