@@ -21,6 +21,9 @@ EXPORTS = (
     "llmint8_matmul_int8",
     "llmint8_matmul_w8",
     "llmint8_pack_w16_rows",
+    "llmint8_quantize_weight_bf16",
+    "llmint8_matmul_bf16",
+    "llmint8_matmul_i32_bf16",
     "llmint8_matmul_i32",
     "llmint8_xpass",
     "llmint8_gemm",
@@ -58,6 +61,9 @@ def load() -> ctypes.CDLL:
         lib.llmint8_matmul_int8.argtypes = [P, I, I, I, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_w8.argtypes = [P, I, I, I, F, P, P, P, P, P, I, P, P, Z, P]
         lib.llmint8_pack_w16_rows.argtypes = [P, I, I, P, I, P, P, P]
+        lib.llmint8_quantize_weight_bf16.argtypes = [P, I, I, P, P, P, P]
+        lib.llmint8_matmul_bf16.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
+        lib.llmint8_matmul_i32_bf16.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_i32.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
         lib.llmint8_xpass.argtypes = [P, I, I, I, F, P, Z, P]
         lib.llmint8_gemm.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
@@ -68,7 +74,8 @@ def load() -> ctypes.CDLL:
         lib.llmint8_device_status.argtypes = [P, P]
         lib.llmint8_selftest_timeout.argtypes = [P, I, P]
         for f in ("llmint8_quantize_weight", "llmint8_matmul", "llmint8_matmul_int8", "llmint8_matmul_i32",
-                  "llmint8_matmul_w8", "llmint8_pack_w16_rows",
+                  "llmint8_matmul_w8", "llmint8_pack_w16_rows", "llmint8_quantize_weight_bf16",
+                  "llmint8_matmul_bf16", "llmint8_matmul_i32_bf16",
                   "llmint8_xpass", "llmint8_gemm", "llmint8_matmul_noalloc", "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
             getattr(lib, f).restype = I
         _lib = lib

@@ -97,6 +97,27 @@ def llmint8_quantize_weight(W: torch.Tensor, Wq=None, colScaleW=None, Wq16=None,
     return Wq, colScaleW, Wq16
 
 
+def llmint8_quantize_weight_bf16(W: torch.Tensor, Wq=None, colScaleW=None, Wq16=None, fp16_codes: bool = True,
+                                 stream=None):
+    """A0 for bf16 W [K, N] -> (Wq int8 [N, K], colScaleW fp32 [N], Wq16 fp16 codes [N, K] or None)."""
+    K, N = W.shape
+    dev = W.device
+    if Wq is None:
+        Wq = torch.empty((N, K), dtype=torch.int8, device=dev)
+    if colScaleW is None:
+        colScaleW = torch.empty((N,), dtype=torch.float32, device=dev)
+    if Wq16 is None and fp16_codes:
+        Wq16 = torch.empty((N, K), dtype=torch.float16, device=dev)
+    _need(W, torch.bfloat16, (K, N), "W")
+    _need(Wq, torch.int8, (N, K), "Wq")
+    _need(colScaleW, torch.float32, (N,), "colScaleW")
+    _need(Wq16, torch.float16, (N, K), "Wq16")
+    st = _lib.load().llmint8_quantize_weight_bf16(_ptr(W), K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
+                                                  _stream(stream, W))
+    _check(st, "llmint8_quantize_weight_bf16")
+    return Wq, colScaleW, Wq16
+
+
 def _shapes(X, Wq):
     M, K = X.shape
     N = Wq.shape[0]
@@ -150,6 +171,38 @@ def llmint8_matmul_w8(X, threshold, Wq, colScaleW, Wq16, W16c=None, row_map=None
                                        workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul_w8")
     return Y
+
+
+def llmint8_matmul_bf16(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspace=None, stream=None):
+    """A1..A5 on bf16 X [M, K] and W16 [K, N] -> Y bf16 [M, N]."""
+    M, K, N = _shapes(X, Wq)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if workspace is None:
+        workspace = make_workspace(M, K, N, X.device)
+    _need(X, torch.bfloat16, (M, K), "X")
+    _need(Y, torch.bfloat16, (M, N), "Y")
+    _need(W16, torch.bfloat16, (K, N), "W16")
+    st = _lib.load().llmint8_matmul_bf16(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
+                                         _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream, X))
+    _check(st, "llmint8_matmul_bf16")
+    return Y
+
+
+def llmint8_matmul_i32_bf16(X, threshold, Wq, colScaleW, Wq16, C=None, workspace=None, stream=None):
+    """The exact int32 accumulator C of llmint8_matmul_bf16 (bf16 X)."""
+    M, K, N = _shapes(X, Wq)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.int32, device=X.device)
+    if workspace is None:
+        workspace = make_workspace(M, K, N, X.device)
+    _need(X, torch.bfloat16, (M, K), "X")
+    _need(C, torch.int32, (M, N), "C")
+    st = _lib.load().llmint8_matmul_i32_bf16(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW),
+                                             _ptr(Wq16), _ptr(C), _ptr(workspace), workspace.numel(),
+                                             _stream(stream, X))
+    _check(st, "llmint8_matmul_i32_bf16")
+    return C
 
 
 def llmint8_matmul_int8(X, Wq, colScaleW, Wq16, Y=None, workspace=None, stream=None):

@@ -28,9 +28,10 @@ struct DeviceInfo {
     bool probed = false;
     bool supported = false;
     int sms = 0;
-    bool gemm_attr_set = false;
-    bool gemv_attr_set = false;
-    bool rowq_cluster_attr_set = false;
+    // kernel attributes set on this device, per element format (0 fp16, 1 bf16)
+    bool gemm_attr_set[2] = {false, false};
+    bool gemv_attr_set[2] = {false, false};
+    bool rowq_cluster_attr_set[2] = {false, false};
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -244,6 +245,7 @@ bool rowq_gathers_w16(bool decode, int K, float threshold, bool write_i32, const
 }
 
 // A1 + A2 into the workspace; with gather_w16 also the A4 operand W16oT.
+template <typename T>
 llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* workspace, const Layout& L,
                             DeviceInfo* dev, cudaStream_t s, const void* W16 = nullptr, int N = 0,
                             bool gather_w16 = false) {
@@ -270,7 +272,7 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
     if (use_outliers && !cluster) {
         if (gy > 1 && cudaMemsetAsync(static_cast<uint8_t*>(workspace) + L.hdr, 0, L.idx - L.hdr, s) != cudaSuccess)
             return LLMINT8_ECUDA;
-        st = launch(k_outlier_scan, dim3(gx, gy), dim3(kScanThreads), 0, s, true, Xh, M, K, threshold, w.bitmap,
+        st = launch(k_outlier_scan<T>, dim3(gx, gy), dim3(kScanThreads), 0, s, true, Xh, M, K, threshold, w.bitmap,
                     gy > 1 ? nullptr : w.hdr);
         if (st != LLMINT8_OK) return st;
     }
@@ -296,18 +298,18 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
     if (cluster) {
         {
             std::lock_guard<std::mutex> lock(g_mu);
-            if (!dev->rowq_cluster_attr_set) {  // clusters of up to 16 CTAs (M <= 16)
-                if (cudaFuncSetAttribute(k_row_quant<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            if (!dev->rowq_cluster_attr_set[Fmt<T>::kBF16]) {  // clusters of up to 16 CTAs (M <= 16)
+                if (cudaFuncSetAttribute(k_row_quant<1, T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
                         cudaSuccess ||
-                    cudaFuncSetAttribute(k_row_quant<2>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                    cudaFuncSetAttribute(k_row_quant<2, T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
                         cudaSuccess)
                     return LLMINT8_ECUDA;
-                dev->rowq_cluster_attr_set = true;
+                dev->rowq_cluster_attr_set[Fmt<T>::kBF16] = true;
             }
         }
         const unsigned cm = (unsigned)M;
-        return row_quant_vpt(K) == 1 ? launch_cluster(k_row_quant<1>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra)
-                                     : launch_cluster(k_row_quant<2>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra);
+        return row_quant_vpt(K) == 1 ? launch_cluster(k_row_quant<1, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra)
+                                     : launch_cluster(k_row_quant<2, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra);
     }
     ra.W16 = gather_w16 ? static_cast<const __half*>(W16) : nullptr;
     ra.N = N;
@@ -315,20 +317,21 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
     ra.w16o_pitch = L.kp;
     if (!L.decode && K <= 4096) {  // many short rows: one warp per row
         const dim3 grid((M + kRowsPerCta - 1) / kRowsPerCta), block(kRowsPerCta * 32);
-        if (K <= 1024) return launch(k_row_quant_warp<4>, grid, block, 0, s, pdl, ra);
-        if (K <= 2048) return launch(k_row_quant_warp<8>, grid, block, 0, s, pdl, ra);
-        return launch(k_row_quant_warp<16>, grid, block, 0, s, pdl, ra);
+        if (K <= 1024) return launch(k_row_quant_warp<4, T>, grid, block, 0, s, pdl, ra);
+        if (K <= 2048) return launch(k_row_quant_warp<8, T>, grid, block, 0, s, pdl, ra);
+        return launch(k_row_quant_warp<16, T>, grid, block, 0, s, pdl, ra);
     }
     switch (row_quant_vpt(K)) {
-        case 1: return launch(k_row_quant<1>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
-        case 2: return launch(k_row_quant<2>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
-        case 4: return launch(k_row_quant<4>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
-        case 8: return launch(k_row_quant<8>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
-        default: return launch(k_row_quant<0>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
+        case 1: return launch(k_row_quant<1, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
+        case 2: return launch(k_row_quant<2, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
+        case 4: return launch(k_row_quant<4, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
+        case 8: return launch(k_row_quant<8, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
+        default: return launch(k_row_quant<0, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
     }
 }
 
 // A3 + A4 + A5 from the workspace an xpass_launch of the same problem filled.
+template <typename T>
 llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
                            const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
                            void* workspace, const Layout& L, DeviceInfo* dev, cudaStream_t s,
@@ -361,22 +364,22 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         ga.w16_rows = src.rows;
         {
             std::lock_guard<std::mutex> lock(g_mu);
-            if (!dev->gemv_attr_set) {
+            if (!dev->gemv_attr_set[Fmt<T>::kBF16]) {
                 const int m8 = (int)gemv_dyn_smem(8), m16 = (int)gemv_dyn_smem(16);
-                if (cudaFuncSetAttribute(k_gemv_decode<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
+                if (cudaFuncSetAttribute(k_gemv_decode<1, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
                         cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
+                    cudaFuncSetAttribute(k_gemv_decode<1, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
                         cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
+                    cudaFuncSetAttribute(k_gemv_decode<2, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
                         cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
+                    cudaFuncSetAttribute(k_gemv_decode<2, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
                         cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          m8) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          m8) != cudaSuccess)
                     return LLMINT8_ECUDA;
-                dev->gemv_attr_set = true;
+                dev->gemv_attr_set[Fmt<T>::kBF16] = true;
             }
         }
         const dim3 block(kGemvWarps * 32);
@@ -384,24 +387,24 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         if (M <= 8) {
             if (ntiles > slots) {  // one-tile CTAs would need several waves: persistent grid
                 const dim3 grid(slots);
-                return write_i32 ? launch(k_gemv_decode_tiles<1, true>, grid, block, gemv_dyn_smem(M), s, true, ga)
-                                 : launch(k_gemv_decode_tiles<1, false>, grid, block, gemv_dyn_smem(M), s, true, ga);
+                return write_i32 ? launch(k_gemv_decode_tiles<1, true, T>, grid, block, gemv_dyn_smem(M), s, true, ga)
+                                 : launch(k_gemv_decode_tiles<1, false, T>, grid, block, gemv_dyn_smem(M), s, true, ga);
             }
             const dim3 grid(ntiles);
-            return write_i32 ? launch(k_gemv_decode<1, true>, grid, block, gemv_dyn_smem(M), s, true, ga)
-                             : launch(k_gemv_decode<1, false>, grid, block, gemv_dyn_smem(M), s, true, ga);
+            return write_i32 ? launch(k_gemv_decode<1, true, T>, grid, block, gemv_dyn_smem(M), s, true, ga)
+                             : launch(k_gemv_decode<1, false, T>, grid, block, gemv_dyn_smem(M), s, true, ga);
         }
         // up to 16 rows: the persistent form measured slower (its per-tile
         // epilogue costs more than the waves it removes), one-tile CTAs
         const dim3 grid(ntiles);
-        return write_i32 ? launch(k_gemv_decode<2, true>, grid, block, gemv_dyn_smem(M), s, true, ga)
-                         : launch(k_gemv_decode<2, false>, grid, block, gemv_dyn_smem(M), s, true, ga);
+        return write_i32 ? launch(k_gemv_decode<2, true, T>, grid, block, gemv_dyn_smem(M), s, true, ga)
+                         : launch(k_gemv_decode<2, false, T>, grid, block, gemv_dyn_smem(M), s, true, ga);
     }
 
     // A4 operand: gathered, transposed outlier rows of W16 (unless the X pass wrote it)
     if (use_outliers && !write_i32 && !w16o_ready) {
         const W8Rows w8{src.W16c, src.row_map, src.rows, Wq, K, colScaleW};
-        st = launch(k_gather_w16_outlier_rows, dim3((N + 63) / 64), dim3(256), 0, s, true,
+        st = launch(k_gather_w16_outlier_rows<T>, dim3((N + 63) / 64), dim3(256), 0, s, true,
                     src.w8 ? nullptr : static_cast<const __half*>(W16), N, (const WsHeader*)w.hdr,
                     (const int32_t*)w.idx, w.w16o, L.kp, w8);
         if (st != LLMINT8_OK) return st;
@@ -418,17 +421,17 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
     if ((st = encode_fp16_2d(&tm_wo, w.w16o, N, L.kp, L.kp, b_rows)) != LLMINT8_OK) return st;
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!dev->gemm_attr_set) {
-            if (cudaFuncSetAttribute(k_gemm_tc<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (!dev->gemm_attr_set[Fmt<T>::kBF16]) {
+            if (cudaFuncSetAttribute(k_gemm_tc<false, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kGemmSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(k_gemm_tc<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                cudaFuncSetAttribute(k_gemm_tc<true, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kGemmSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(k_gemm_tc<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                cudaFuncSetAttribute(k_gemm_tc<false, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kGemmSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(k_gemm_tc<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                cudaFuncSetAttribute(k_gemm_tc<true, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kGemmSmem) != cudaSuccess)
                 return LLMINT8_ECUDA;
-            dev->gemm_attr_set = true;
+            dev->gemm_attr_set[Fmt<T>::kBF16] = true;
         }
     }
     GemmArgs ga;
@@ -448,17 +451,17 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         const int clusters = units < dev->sms / 2 ? units : dev->sms / 2;
         const dim3 grid(2 * clusters);
         if (write_i32)
-            return launch_cluster(k_gemm_tc<true, true>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u, tm_a, tm_b,
+            return launch_cluster(k_gemm_tc<true, true, T>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u, tm_a, tm_b,
                                   tm_xo, tm_wo, ga);
-        return launch_cluster(k_gemm_tc<false, true>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u, tm_a, tm_b,
+        return launch_cluster(k_gemm_tc<false, true, T>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u, tm_a, tm_b,
                               tm_xo, tm_wo, ga);
     }
     const int ntiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
     const int grid = ntiles < dev->sms ? ntiles : dev->sms;
     if (write_i32)
-        return launch(k_gemm_tc<true, false>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo,
+        return launch(k_gemm_tc<true, false, T>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo,
                       tm_wo, ga);
-    return launch(k_gemm_tc<false, false>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo,
+    return launch(k_gemm_tc<false, false, T>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo,
                   tm_wo, ga);
 }
 
@@ -477,7 +480,8 @@ int kernels_per_call(int M, int K, int N, float threshold, bool write_i32) {
 
 llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
                            const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
-                           void* workspace, size_t ws_bytes, void* stream, const W16Src& src = W16Src()) {
+                           void* workspace, size_t ws_bytes, void* stream, const W16Src& src = W16Src(),
+                           bool bf16 = false) {
     Layout L;
     DeviceInfo* dev = nullptr;
     llmint8_status st = check_common(X, M, K, N, threshold, workspace, ws_bytes, &L, &dev);
@@ -487,9 +491,16 @@ llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the row quantization gathers only from a full fp16 copy (W16 is null in w8 mode)
     const bool gw = !src.w8 && rowq_gathers_w16(L.decode, K, threshold, write_i32, W16);
-    if ((st = xpass_launch(X, M, K, threshold, workspace, L, dev, s, W16, N, gw)) != LLMINT8_OK) return st;
-    return gemm_launch(X, M, K, N, threshold, Wq, colScaleW, Wq16, src.w8 ? nullptr : W16, out, write_i32, workspace,
-                       L, dev, s, gw, src);
+    const void* W16g = src.w8 ? nullptr : W16;
+    if (bf16) {
+        if ((st = xpass_launch<__nv_bfloat16>(X, M, K, threshold, workspace, L, dev, s, W16, N, gw)) != LLMINT8_OK)
+            return st;
+        return gemm_launch<__nv_bfloat16>(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16g, out, write_i32,
+                                          workspace, L, dev, s, gw, src);
+    }
+    if ((st = xpass_launch<__half>(X, M, K, threshold, workspace, L, dev, s, W16, N, gw)) != LLMINT8_OK) return st;
+    return gemm_launch<__half>(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16g, out, write_i32, workspace, L, dev,
+                               s, gw, src);
 }
 
 // Waits on a barrier nothing completes, bounded by spin_limit polls, then
@@ -510,6 +521,31 @@ __global__ void k_selftest_timeout(WsHeader* hdr, uint32_t spin_limit) {
 
 }  // namespace
 
+// A0 for W of element format T (fp16 or bf16)
+template <typename T>
+llmint8_status quantize_weight_impl(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* Wq16,
+                                    void* stream) {
+    if (!W || !Wq || !colScaleW) return LLMINT8_EINVAL;
+    if (K < 1 || N < 1 || K > (1 << 30) || N > (1 << 30)) return LLMINT8_EINVAL;
+    if ((K % 16) || (N % 16)) return LLMINT8_EALIGN;
+    if (!aligned16(W) || !aligned16(Wq) || !aligned16(colScaleW) || (Wq16 && !aligned16(Wq16))) return LLMINT8_EALIGN;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = current_device(&dev);
+    if (st != LLMINT8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(colScaleW, 0, (size_t)N * 4, s) != cudaSuccess) return LLMINT8_ECUDA;
+    const int gx = (N + 255) / 256;
+    int gy = (K + 7) / 8;
+    const int cap = (dev->sms * 8 + gx - 1) / gx;
+    if (gy > cap) gy = cap;
+    if (gy < 1) gy = 1;
+    k_col_absmax<T><<<dim3(gx, gy), 256, 0, s>>>(static_cast<const __half*>(W), K, N, colScaleW);
+    if ((st = launch_status()) != LLMINT8_OK) return st;
+    k_quantize_weight_tile<T><<<dim3((N + 63) / 64, (K + 63) / 64), 256, 0, s>>>(
+        static_cast<const __half*>(W), K, N, colScaleW, Wq, static_cast<__half*>(Wq16));
+    return launch_status();
+}
+
 extern "C" {
 
 const char* llmint8_status_str(int status) {
@@ -527,25 +563,26 @@ const char* llmint8_status_str(int status) {
 
 llmint8_status llmint8_quantize_weight(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* Wq16,
                                        void* stream) {
-    if (!W || !Wq || !colScaleW) return LLMINT8_EINVAL;
-    if (K < 1 || N < 1 || K > (1 << 30) || N > (1 << 30)) return LLMINT8_EINVAL;
-    if ((K % 16) || (N % 16)) return LLMINT8_EALIGN;
-    if (!aligned16(W) || !aligned16(Wq) || !aligned16(colScaleW) || (Wq16 && !aligned16(Wq16))) return LLMINT8_EALIGN;
-    DeviceInfo* dev = nullptr;
-    llmint8_status st = current_device(&dev);
-    if (st != LLMINT8_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(colScaleW, 0, (size_t)N * 4, s) != cudaSuccess) return LLMINT8_ECUDA;
-    const int gx = (N + 255) / 256;
-    int gy = (K + 7) / 8;
-    const int cap = (dev->sms * 8 + gx - 1) / gx;
-    if (gy > cap) gy = cap;
-    if (gy < 1) gy = 1;
-    k_col_absmax<<<dim3(gx, gy), 256, 0, s>>>(static_cast<const __half*>(W), K, N, colScaleW);
-    if ((st = launch_status()) != LLMINT8_OK) return st;
-    k_quantize_weight_tile<<<dim3((N + 63) / 64, (K + 63) / 64), 256, 0, s>>>(
-        static_cast<const __half*>(W), K, N, colScaleW, Wq, static_cast<__half*>(Wq16));
-    return launch_status();
+    return quantize_weight_impl<__half>(W, K, N, Wq, colScaleW, Wq16, stream);
+}
+
+llmint8_status llmint8_quantize_weight_bf16(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* Wq16,
+                                            void* stream) {
+    return quantize_weight_impl<__nv_bfloat16>(W, K, N, Wq, colScaleW, Wq16, stream);
+}
+
+llmint8_status llmint8_matmul_bf16(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
+                                   const float* colScaleW, const void* Wq16, const void* W16, void* Y, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, workspace_bytes,
+                       stream, W16Src(), true);
+}
+
+llmint8_status llmint8_matmul_i32_bf16(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
+                                       const float* colScaleW, const void* Wq16, int32_t* C, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, nullptr, C, true, workspace, workspace_bytes,
+                       stream, W16Src(), true);
 }
 
 size_t llmint8_workspace_bytes(int M, int K, int N) {
@@ -613,7 +650,7 @@ llmint8_status llmint8_xpass(const void* X, int M, int K, int N, float threshold
     llmint8_status st = check_common(X, M, K, N, threshold, workspace, workspace_bytes, &L, &dev);
     if (st != LLMINT8_OK) return st;
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
-    return xpass_launch(X, M, K, threshold, workspace, L, dev, static_cast<cudaStream_t>(stream));
+    return xpass_launch<__half>(X, M, K, threshold, workspace, L, dev, static_cast<cudaStream_t>(stream));
 }
 
 llmint8_status llmint8_gemm(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
@@ -625,7 +662,7 @@ llmint8_status llmint8_gemm(const void* X, int M, int K, int N, float threshold,
     if (st != LLMINT8_OK) return st;
     if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, Y, false)) != LLMINT8_OK) return st;
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
-    return gemm_launch(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, L, dev,
+    return gemm_launch<__half>(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, L, dev,
                        static_cast<cudaStream_t>(stream));
 }
 

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -99,11 +100,52 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
 
+// 16-bit element formats of X, W and Y: fp16 (__half) or bf16 (__nv_bfloat16).
+// Wherever no arithmetic touches them the values are moved as raw 16-bit words
+// (held in __half-typed storage); Fmt<T> converts at the few places that compute.
+template <typename T>
+struct Fmt;
+template <>
+struct Fmt<__half> {
+    static constexpr bool kBF16 = false;
+    __device__ __forceinline__ static float2 to_float2(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    }
+    __device__ __forceinline__ static float to_float(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+    __device__ __forceinline__ static uint16_t from_float(float f) { return __half_as_ushort(__float2half_rn(f)); }
+    __device__ __forceinline__ static uint32_t pack2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+template <>
+struct Fmt<__nv_bfloat16> {  // bf16 = the upper half of a binary32
+    static constexpr bool kBF16 = true;
+    __device__ __forceinline__ static float2 to_float2(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    __device__ __forceinline__ static float to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+    __device__ __forceinline__ static uint16_t from_float(float f) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+    }
+    __device__ __forceinline__ static uint32_t pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+// the value of a raw 16-bit word of format T
+template <typename T>
+__device__ __forceinline__ float elem_f(__half raw) {
+    return Fmt<T>::to_float(__half_as_ushort(raw));
+}
+
 // A4 weight without a full fp16 copy of W: code q of a column whose absmax is
-// s_w, dequantized as fp16(fp32(q) * fp32(s_w / 127)), each step rounded to
-// nearest even (a code times its scale, the scale stored as the absmax).
+// s_w, dequantized as RNE_T(fp32(q) * fp32(s_w / 127)), each step rounded to
+// nearest even (a code times its scale, the scale stored as the absmax); the
+// raw 16-bit word of format T.
+template <typename T>
 __device__ __forceinline__ __half dequant_weight(int8_t q, float s_w) {
-    return __float2half_rn(__fmul_rn((float)q, __fdiv_rn(s_w, 127.0f)));
+    return __ushort_as_half(Fmt<T>::from_float(__fmul_rn((float)q, __fdiv_rn(s_w, 127.0f))));
 }
 
 // Hint: bring [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
@@ -322,12 +364,12 @@ __device__ __forceinline__ uint64_t make_sdesc_k128(uint32_t smem_addr) {
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B, fp32 D,
-// both operands K-major, shape M x N.
-__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N) {
+// Instruction descriptor of tcgen05.mma kind::f16: fp16 (or, with bf16, bf16)
+// A and B, fp32 D, both operands K-major, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool bf16 = false) {
     return (1u << 4)                          // D format: f32
-           | (0u << 7)                        // A format: f16
-           | (0u << 10)                       // B format: f16
+           | ((bf16 ? 1u : 0u) << 7)          // A format: f16 (0) or bf16 (1)
+           | ((bf16 ? 1u : 0u) << 10)         // B format: f16 (0) or bf16 (1)
            | (0u << 15) | (0u << 16)          // A, B K-major
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16

@@ -75,7 +75,7 @@ struct GemmSmem {
     uint32_t abort_flag;
 };
 
-template <bool WRITE_I32, bool PAIR>
+template <bool WRITE_I32, bool PAIR, typename T>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_wo, GemmArgs a) {
@@ -215,6 +215,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // (pairs: the first CTA's thread issues for both)
         if (lane == 0 && rank == 0) {
             constexpr uint32_t idesc = make_idesc_f16(PAIR ? 2 * kBM : kBM, kBN);
+            // the outlier chunk multiplies the gathered X and W values, of format T
+            constexpr uint32_t idesc_o = make_idesc_f16(PAIR ? 2 * kBM : kBM, kBN, Fmt<T>::kBF16);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t chunk = 0;
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int s_begin = ch < nchunks_int ? ch * kChunkSteps : ksteps;
                     const int s_end = ch < nchunks_int ? min(ksteps, s_begin + kChunkSteps) : ksteps + osteps;
                     const uint32_t d_tmem = tmem_base + b * (uint32_t)kBN;
+                    const uint32_t id = ch < nchunks_int ? idesc : idesc_o;
                     for (int s = s_begin; s < s_end; ++s) {
                         if (!wait_bar(&ss->full[stage], phase)) {
                             fail(3);
@@ -246,9 +249,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             // advance 16 fp16 = 32 bytes inside the 128-byte swizzled row
                             const uint32_t acc = (s > s_begin || kk > 0) ? 1u : 0u;
                             if constexpr (PAIR)
-                                tc_mma_f16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, acc);
+                                tc_mma_f16_pair(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), id, acc);
                             else
-                                tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, acc);
+                                tc_mma_f16(d_tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), id, acc);
                         }
                         if constexpr (PAIR)
                             tc_commit_pair(&ss->empty[stage], 0x3);  // both CTAs' stage is free
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                     make_int4(sum[j * 16 + v * 4], sum[j * 16 + v * 4 + 1], sum[j * 16 + v * 4 + 2],
                                               sum[j * 16 + v * 4 + 3]);
                     } else {
-                        __half* orow = reinterpret_cast<__half*>(a.out) + (size_t)row * a.N;
+                        uint16_t* orow = reinterpret_cast<uint16_t*>(a.out) + (size_t)row * a.N;
 #pragma unroll
                         for (int v = 0; v < 2; ++v) {
                             const int c8 = cb + v * 8;
@@ -365,8 +368,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                     const float y0 = fmaf((float)sum[j * 16 + c], sx * sw[2 * e], __uint_as_float(r[c]));
                                     const float y1 =
                                         fmaf((float)sum[j * 16 + c + 1], sx * sw[2 * e + 1], __uint_as_float(r[c + 1]));
-                                    __half2 hv = __floats2half2_rn(y0, y1);
-                                    o[e] = *reinterpret_cast<uint32_t*>(&hv);
+                                    o[e] = Fmt<T>::pack2(y0, y1);
                                 }
                                 *reinterpret_cast<uint4*>(orow + c8) = make_uint4(o[0], o[1], o[2], o[3]);
                             }

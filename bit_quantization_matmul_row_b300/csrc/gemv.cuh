@@ -86,6 +86,7 @@ __device__ __forceinline__ int ldg_nc_s8(const int8_t* p) {
     return v;
 }
 
+template <typename T>
 __device__ __forceinline__ void stage_w16_8(const GemvArgs& a, __half* dst, int k, int nb, W8Pending& pend) {
     if (!a.w8) {
         cp_async16(dst, a.W16 + (size_t)k * a.N + nb);
@@ -102,13 +103,14 @@ __device__ __forceinline__ void stage_w16_8(const GemvArgs& a, __half* dst, int 
     pend.nb = nb;
 }
 
+template <typename T>
 __device__ __forceinline__ void w8_finish(const GemvArgs& a, W8Pending& pend) {
     if (pend.dst == nullptr) return;
     uint32_t h[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const __half lo = dequant_weight((int8_t)pend.q[2 * e], a.col_scale[pend.nb + 2 * e]);
-        const __half hi = dequant_weight((int8_t)pend.q[2 * e + 1], a.col_scale[pend.nb + 2 * e + 1]);
+        const __half lo = dequant_weight<T>((int8_t)pend.q[2 * e], a.col_scale[pend.nb + 2 * e]);
+        const __half hi = dequant_weight<T>((int8_t)pend.q[2 * e + 1], a.col_scale[pend.nb + 2 * e + 1]);
         h[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
     }
     *reinterpret_cast<uint4*>(pend.dst) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -116,11 +118,12 @@ __device__ __forceinline__ void w8_finish(const GemvArgs& a, W8Pending& pend) {
 }
 
 // One element of row k of W (the A4 operand) at column n, from the same sources.
+template <typename T>
 __device__ __forceinline__ float w16_value(const GemvArgs& a, int k, int n) {
-    if (!a.w8) return __half2float(a.W16[(size_t)k * a.N + n]);
+    if (!a.w8) return elem_f<T>(a.W16[(size_t)k * a.N + n]);
     const int rm = a.row_map != nullptr ? __ldg(a.row_map + k) : -1;
-    if (rm >= 0 && rm < a.w16_rows) return __half2float(a.W16c[(size_t)rm * a.N + n]);
-    return __half2float(dequant_weight(a.Wq[(size_t)n * a.K + k], a.col_scale[n]));
+    if (rm >= 0 && rm < a.w16_rows) return elem_f<T>(a.W16c[(size_t)rm * a.N + n]);
+    return elem_f<T>(dequant_weight<T>(a.Wq[(size_t)n * a.K + k], a.col_scale[n]));
 }
 
 __device__ __forceinline__ void imma_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -148,7 +151,7 @@ __device__ __forceinline__ void imma_16832(int (&d)[4], uint32_t a0, uint32_t a1
 // Commit groups: one per weight step before the wait (R), the X halves of those
 // R steps (one group), the outlier staging (one group), then one group per
 // refilled step.
-template <int MT, bool WRITE_I32>
+template <int MT, bool WRITE_I32, typename T>
 __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) {
     constexpr int R = gemv_ring(MT);
     const int SLOT = gemv_slot(a.M);
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
         for (int e = tid; e < 2 * nidx; e += kGemvWarps * 32) {
             const int j = e >> 1, hv = e & 1;
             const int k = base == 0 ? k_first : (base + j < K ? __ldcg(a.outlier_idx + base + j) : 0);
-            if (j < c) stage_w16_8(a, &s_w16o[j][hv * 8], k, n0 + hv * 8, pend);
+            if (j < c) stage_w16_8<T>(a, &s_w16o[j][hv * 8], k, n0 + hv * 8, pend);
         }
         const int cv = (c + 7) >> 3;
         for (int e = tid; e < a.M * (kGemvOutChunk / 8); e += kGemvWarps * 32) {
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
     // No copy may still target shared memory: the ring is drained (its later
     // groups are empty) and the staging group has landed.  Each warp's partials
     // then go to its own ring, [16 x rows][16 columns] int32.
-    w8_finish(a, pend);
+    w8_finish<T>(a, pend);
     cp_async_wait_all();
     int32_t* red = reinterpret_cast<int32_t*>(ring);
     // accumulator layout: d0,d1 -> (column g, x rows 8t+2q, +1); d2,d3 -> (column g+8, same rows)
@@ -323,19 +326,19 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
         for (int base = 0;;) {
             const int cc = min(kGemvOutChunk, cnt - base);
             if (active)
-                for (int j = 0; j < cc; ++j) f = fmaf(__half2float(s_xo[ri][j]), __half2float(s_w16o[j][nl]), f);
+                for (int j = 0; j < cc; ++j) f = fmaf(elem_f<T>(s_xo[ri][j]), elem_f<T>(s_w16o[j][nl]), f);
             base += kGemvOutChunk;
             if (base >= cnt) break;
             __syncthreads();
             stage_outliers(base, min(kGemvOutChunk, cnt - base));
-            w8_finish(a, pend);
+            w8_finish<T>(a, pend);
             cp_async_wait_all();
             __syncthreads();
         }
     }
     if (active) {
         const float scale = rs * cs * (1.0f / 16129.0f);
-        reinterpret_cast<__half*>(a.out)[(size_t)ri * a.N + n] = __float2half_rn(fmaf((float)c, scale, f));
+        reinterpret_cast<uint16_t*>(a.out)[(size_t)ri * a.N + n] = Fmt<T>::from_float(fmaf((float)c, scale, f));
     }
 }
 
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode(GemvArgs a) 
 // staging of the next tile.
 constexpr int kTileOutChunk = 64;
 
-template <int MT, bool WRITE_I32>
+template <int MT, bool WRITE_I32, typename T>
 __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode_tiles(GemvArgs a) {
     constexpr int R = gemv_ring(MT);
     constexpr int MR = 8 * MT;  // rows of X held by the fragments
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode_tiles(GemvAr
     auto stage_w16 = [&](int buf, int n0) {
         for (int e = tid; e < 2 * cst; e += kGemvWarps * 32) {
             const int jx = e >> 1, hv = e & 1;
-            stage_w16_8(a, &s_w16o[buf][jx][hv * 8], s_idx[jx], n0 + hv * 8, pend);
+            stage_w16_8<T>(a, &s_w16o[buf][jx][hv * 8], s_idx[jx], n0 + hv * 8, pend);
         }
         cp_async_commit();
     };
@@ -527,7 +530,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode_tiles(GemvAr
             cp_async_wait_group<R - 1>();
         else
             cp_async_wait_all();
-        w8_finish(a, pend);
+        w8_finish<T>(a, pend);
         __syncthreads();  // partials and staged operands visible to all
         // the other staging buffer was last read by the previous tile's
         // epilogue, which every thread finished before the barrier ending it
@@ -544,14 +547,14 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 2) k_gemv_decode_tiles(GemvAr
         } else if (active) {
             float f = 0.0f;
             for (int jj = 0; jj < cst; ++jj)
-                f = fmaf(__half2float(s_xo[ri][jj]), __half2float(s_w16o[j & 1][jj][nl]), f);
+                f = fmaf(elem_f<T>(s_xo[ri][jj]), elem_f<T>(s_w16o[j & 1][jj][nl]), f);
             for (int jj = cst; jj < cnt; ++jj) {  // past the staged chunk: through L2
                 const int k = __ldcg(a.outlier_idx + jj);
                 const __half xv = __ldcg(a.xo + (size_t)ri * a.xo_pitch + jj);
-                f = fmaf(__half2float(xv), w16_value(a, k, n), f);
+                f = fmaf(elem_f<T>(xv), w16_value<T>(a, k, n), f);
             }
             const float scale = rs * cs * (1.0f / 16129.0f);
-            reinterpret_cast<__half*>(a.out)[(size_t)ri * a.N + n] = __float2half_rn(fmaf((float)c, scale, f));
+            reinterpret_cast<uint16_t*>(a.out)[(size_t)ri * a.N + n] = Fmt<T>::from_float(fmaf((float)c, scale, f));
         }
         __syncthreads();  // s_red and this tile's staging buffer may be overwritten
     }

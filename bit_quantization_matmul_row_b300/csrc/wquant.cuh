@@ -17,6 +17,7 @@ namespace llmint8 {
 // Column absmax, pass 1: each CTA reduces a 256-column strip over a slice of
 // rows and folds its result into colScaleW with an integer atomicMax (valid for
 // non-negative floats).  colScaleW must be zero on entry.
+template <typename T>
 __global__ void __launch_bounds__(256) k_col_absmax(const __half* __restrict__ W, int K, int N,
                                                     float* __restrict__ col_amax) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -28,7 +29,7 @@ __global__ void __launch_bounds__(256) k_col_absmax(const __half* __restrict__ W
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                const float2 f = Fmt<T>::to_float2(w[e]);
                 m[2 * e] = fmaxf(m[2 * e], fabsf(f.x));
                 m[2 * e + 1] = fmaxf(m[2 * e + 1], fabsf(f.y));
             }
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(256) k_col_absmax(const __half* __restrict__ W
 }
 
 // Pass 2: quantize a 64(k) x 64(n) tile and write it transposed.
+template <typename T>
 __global__ void __launch_bounds__(256) k_quantize_weight_tile(const __half* __restrict__ W, int K, int N,
                                                               const float* __restrict__ col_amax,
                                                               int8_t* __restrict__ Wq, __half* __restrict__ Wq16) {
@@ -64,7 +66,7 @@ __global__ void __launch_bounds__(256) k_quantize_weight_tile(const __half* __re
         const int kr = e >> 5, nc = (e & 31) * 2;
         const int k = k0 + kr, n = n0 + nc;
         if (k < K && n < N) {  // N % 16 == 0: n and n+1 both valid
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(W + (size_t)k * N + n));
+            const float2 f = Fmt<T>::to_float2(*reinterpret_cast<const uint32_t*>(W + (size_t)k * N + n));
             const float q0 = fminf(fmaxf(roundf(__fmul_rn(f.x, s_sf[nc])), -127.0f), 127.0f);
             const float q1 = fminf(fmaxf(roundf(__fmul_rn(f.y, s_sf[nc + 1])), -127.0f), 127.0f);
             tile[nc][kr] = (int8_t)(int)q0;

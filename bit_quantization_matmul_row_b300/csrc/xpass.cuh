@@ -25,13 +25,14 @@ namespace llmint8 {
 constexpr int kScanThreads = 256;
 constexpr int kScanCols = 256;  // columns per CTA: 32 lanes x 8 fp16
 
-// |x| > t for the 8 fp16 values of a 16-byte vector -> 8-bit mask (bit e = element e).
+// |x| > t for the 8 values (format T) of a 16-byte vector -> 8-bit mask (bit e = element e).
+template <typename T>
 __device__ __forceinline__ uint32_t outlier_mask8(uint4 v, float t) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t m = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        const float2 f = Fmt<T>::to_float2(w[e]);
         m |= (fabsf(f.x) > t ? 1u : 0u) << (2 * e);
         m |= (fabsf(f.y) > t ? 1u : 0u) << (2 * e + 1);
     }
@@ -57,6 +58,7 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // with several, the words are OR-ed atomically and the bitmap must be zero on
 // entry.  `hdr`, when given, has its error word cleared by CTA 0 (the first
 // kernel of a call resets the word).
+template <typename T>
 __global__ void __launch_bounds__(kScanThreads) k_outlier_scan(const __half* __restrict__ X, int M, int K, float t,
                                                                uint32_t* __restrict__ bitmap, WsHeader* hdr) {
     pdl_trigger();
@@ -81,9 +83,9 @@ __global__ void __launch_bounds__(kScanThreads) k_outlier_scan(const __half* __r
 #pragma unroll
             for (int u = 0; u < 4; ++u) x[u] = ldg_cg_v4(p + (size_t)(r + u * step) * K);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) m |= outlier_mask8(x[u], t);
+            for (int u = 0; u < 4; ++u) m |= outlier_mask8<T>(x[u], t);
         }
-        for (; r < M; r += step) m |= outlier_mask8(ldg_cg_v4(p + (size_t)r * K), t);
+        for (; r < M; r += step) m |= outlier_mask8<T>(ldg_cg_v4(p + (size_t)r * K), t);
     }
     // lanes 4w..4w+3 hold the 32 columns of bitmap word w of this strip
     uint32_t word = m << (8 * (lane & 3));
@@ -155,7 +157,7 @@ __device__ __forceinline__ float code_of(float x, float sf) {
 // the columns of its own row (already in registers), pushes that bit map into
 // the shared memory of every CTA of the cluster, and after one cluster barrier
 // ORs the M row maps locally (A1: a column is an outlier when any row exceeds t).
-template <int VPT>
+template <int VPT, typename T>
 __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
     // bit-map words held in shared memory: the whole row when it sits in registers
     constexpr int kWords = VPT > 0 ? (VPT * 64 > kRowThreads ? VPT * 64 : kRowThreads) : kMaxWords;
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
         for (int i = 0; i < (VPT > 0 ? VPT : 1); ++i) {
             const int vi = tid + i * kRowThreads;
             // lanes 4k..4k+3 hold the 4 vectors (32 columns) of bit-map word vi / 4
-            uint32_t word = (vi < nvec ? outlier_mask8(v[i], a.t) : 0u) << (8 * (lane & 3));
+            uint32_t word = (vi < nvec ? outlier_mask8<T>(v[i], a.t) : 0u) << (8 * (lane & 3));
             word |= __shfl_xor_sync(0xffffffffu, word, 1);
             word |= __shfl_xor_sync(0xffffffffu, word, 2);
             if ((lane & 3) == 0 && vi < nvec)
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+            const float2 f = Fmt<T>::to_float2(w[e]);
             if (!((om >> (2 * e)) & 1u)) amax = fmaxf(amax, fabsf(f.x));
             if (!((om >> (2 * e + 1)) & 1u)) amax = fmaxf(amax, fabsf(f.y));
         }
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
         float q[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+            const float2 f = Fmt<T>::to_float2(w[e]);
             q[2 * e] = ((om >> (2 * e)) & 1u) ? 0.0f : code_of(f.x, sf);
             q[2 * e + 1] = ((om >> (2 * e + 1)) & 1u) ? 0.0f : code_of(f.y, sf);
         }
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
 constexpr int kRowsPerCta = 8;
 constexpr int kGatherCols = 16;
 
-template <int VPL>
+template <int VPL, typename T>
 __global__ void __launch_bounds__(kRowsPerCta * 32) k_row_quant_warp(RowQuantArgs a) {
     constexpr int kWords = 8 * VPL;  // bit-map words of a row (<= the CTA's 256 threads)
     static_assert(kWords <= kRowsPerCta * 32, "one bit-map word per thread");
@@ -474,7 +476,7 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) k_row_quant_warp(RowQuantArg
                 const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                    const float2 f = Fmt<T>::to_float2(w[e]);
                     if (!((om >> (2 * e)) & 1u)) amax = fmaxf(amax, fabsf(f.x));
                     if (!((om >> (2 * e + 1)) & 1u)) amax = fmaxf(amax, fabsf(f.y));
                 }
@@ -499,7 +501,7 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) k_row_quant_warp(RowQuantArg
             float q[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                const float2 f = Fmt<T>::to_float2(w[e]);
                 q[2 * e] = ((om >> (2 * e)) & 1u) ? 0.0f : code_of(f.x, sf);
                 q[2 * e + 1] = ((om >> (2 * e + 1)) & 1u) ? 0.0f : code_of(f.y, sf);
             }
@@ -590,6 +592,7 @@ struct W8Rows {
     const float* col_scale;
 };
 
+template <typename T>
 __global__ void __launch_bounds__(256) k_gather_w16_outlier_rows(const __half* __restrict__ W16, int N,
                                                                  const WsHeader* __restrict__ hdr,
                                                                  const int32_t* __restrict__ outlier_idx,
@@ -614,7 +617,7 @@ __global__ void __launch_bounds__(256) k_gather_w16_outlier_rows(const __half* _
                 } else {
                     const int rm = w8.row_map != nullptr ? __ldg(w8.row_map + k) : -1;
                     v = (rm >= 0 && rm < w8.rows) ? w8.W16c[(size_t)rm * N + n]
-                                                  : dequant_weight(w8.Wq[(size_t)n * w8.K + k], w8.col_scale[n]);
+                                                  : dequant_weight<T>(w8.Wq[(size_t)n * w8.K + k], w8.col_scale[n]);
                 }
             }
             tile[pr][nc] = v;

@@ -107,6 +107,24 @@ llmint8_status llmint8_matmul(const void *X, int M, int K, int N, float threshol
                               void *stream);
 
 /*
+ * bfloat16 forms: the same steps on bf16 W, X and Y (all other arguments as the
+ * fp16 entry points).  The codes, scales, outlier test and the int32 product are
+ * computed from the fp32 values of the bf16 inputs exactly as from fp16 ones;
+ * the outlier slice multiplies bf16 X and W values with fp32 accumulation and Y
+ * is rounded to bf16 (nearest even).  Wq16 stays fp16 (exact integer codes).
+ * llmint8_matmul_i32_bf16 writes the int32 accumulator C, as llmint8_matmul_i32.
+ */
+llmint8_status llmint8_quantize_weight_bf16(const void *W, int K, int N, int8_t *Wq, float *colScaleW,
+                                            void *Wq16, void *stream);
+llmint8_status llmint8_matmul_bf16(const void *X, int M, int K, int N, float threshold,
+                                   const int8_t *Wq, const float *colScaleW, const void *Wq16,
+                                   const void *W16, void *Y, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+llmint8_status llmint8_matmul_i32_bf16(const void *X, int M, int K, int N, float threshold,
+                                       const int8_t *Wq, const float *colScaleW, const void *Wq16,
+                                       int32_t *C, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * llmint8_matmul without a full fp16 copy of W (int8 weight storage only).  The
  * outlier slice (A4) needs row k of W for every outlier column k of X: it is
  * W16c[row_map[k], :] when 0 <= row_map[k] < w16_rows (rows the caller chose to

@@ -157,3 +157,13 @@ def test_w8_argument_errors(lib):
     assert lib.llmint8_pack_w16_rows(None, 64, 64, None, 0, None, P(FAKE), None) == _lib.EINVAL
     assert lib.llmint8_pack_w16_rows(P(FAKE), 64, 64, None, 3, P(FAKE), P(FAKE), None) == _lib.EINVAL
     assert lib.llmint8_pack_w16_rows(P(FAKE), 64, 40, None, 0, None, P(FAKE), None) == _lib.EALIGN
+
+
+def test_bf16_argument_errors(lib):
+    from bit_quantization_matmul_row_b300 import _lib
+    P = ctypes.c_void_p
+    assert lib.llmint8_quantize_weight_bf16(P(0), 64, 64, P(FAKE), P(FAKE), None, None) == _lib.EINVAL
+    assert lib.llmint8_quantize_weight_bf16(P(FAKE), 65, 64, P(FAKE), P(FAKE), None, None) == _lib.EALIGN
+    ws = lib.llmint8_workspace_bytes(16, 64, 64)
+    assert lib.llmint8_matmul_bf16(P(FAKE), 16, 64, 64, 6.0, P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), P(FAKE), ws,
+                                   None) == _lib.EINVAL  # finite threshold without W16
