@@ -411,9 +411,13 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
     }
     if ((st = get_encoder()) != LLMINT8_OK) return st;
     // CTA pairs (256 x 256 tiles, each CTA loading 128 columns of B) once M
-    // spans two 128-row tiles
+    // spans two 128-row tiles; 256 x 128 pair tiles when the wide ones would
+    // give fewer clusters than 60 % of the cluster slots (medium M)
     const bool pair = M > kBM && dev->sms >= 2;
-    const int b_rows = pair ? kBN / 2 : kBN;
+    const int tiles_m2 = (M + 2 * kBM - 1) / (2 * kBM);
+    const bool narrow = pair && tiles_m2 * ((N + kBN - 1) / kBN) * 10 < 6 * (dev->sms / 2);
+    const int bn = narrow ? 128 : kBN;
+    const int b_rows = pair ? bn / 2 : bn;
     CUtensorMap tm_a, tm_b, tm_xo, tm_wo;
     if ((st = encode_fp16_2d(&tm_a, w.codes, M, K, K, kBM)) != LLMINT8_OK) return st;
     if ((st = encode_fp16_2d(&tm_b, Wq16, N, K, K, b_rows)) != LLMINT8_OK) return st;
@@ -429,6 +433,10 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
                 cudaFuncSetAttribute(k_gemm_tc<false, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kGemmSmem) != cudaSuccess ||
                 cudaFuncSetAttribute(k_gemm_tc<true, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<false, true, T, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<true, true, T, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kGemmSmem) != cudaSuccess)
                 return LLMINT8_ECUDA;
             dev->gemm_attr_set[Fmt<T>::kBF16] = true;
@@ -447,9 +455,16 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
     ga.use_outliers = (use_outliers && !write_i32) ? 1 : 0;
     ga.spin_limit = kDefaultSpinLimit;
     if (pair) {
-        const int units = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
+        const int units = tiles_m2 * ((N + bn - 1) / bn);
         const int clusters = units < dev->sms / 2 ? units : dev->sms / 2;
         const dim3 grid(2 * clusters);
+        if (narrow) {
+            if (write_i32)
+                return launch_cluster(k_gemm_tc<true, true, T, 128>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u,
+                                      tm_a, tm_b, tm_xo, tm_wo, ga);
+            return launch_cluster(k_gemm_tc<false, true, T, 128>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u,
+                                  tm_a, tm_b, tm_xo, tm_wo, ga);
+        }
         if (write_i32)
             return launch_cluster(k_gemm_tc<true, true, T>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u, tm_a, tm_b,
                                   tm_xo, tm_wo, ga);

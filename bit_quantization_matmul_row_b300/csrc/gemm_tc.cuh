@@ -43,7 +43,7 @@ namespace llmint8 {
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr int kStages = 4;      // one CTA per tile: 48 KB stages
 constexpr int kPairStages = 6;  // CTA pairs: 32 KB stages
-constexpr int kMaxStages = kPairStages;
+constexpr int kMaxStages = 8;   // CTA pairs on 256 x 128 tiles: 24 KB stages
 constexpr int kChunkSteps = 16;  // 16 x 64 = 1024 products per exact fp32 chunk
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 64 + kEpiWarps * 32;
@@ -53,6 +53,16 @@ constexpr uint32_t kPairStageB = kStageB / 2;  // 16 KB: the CTA's half of the B
 constexpr uint32_t kTmemCols = 512;          // two 256-column fp32 accumulators
 static_assert(kStages * (kStageA + kStageB) == kPairStages * (kStageA + kPairStageB), "same ring size");
 constexpr size_t kGemmSmem = 1024 /*align slack*/ + (size_t)kStages * (kStageA + kStageB) + 256;
+
+// Ring depth and B bytes per stage of one CTA for a tile width BN (256, or 128
+// for CTA pairs when wide tiles would leave SMs idle): the rings fill the same
+// 192 KB.
+__host__ __device__ constexpr int gemm_stages(bool pair, int BN) { return !pair ? kStages : BN == 256 ? kPairStages : 8; }
+__host__ __device__ constexpr uint32_t gemm_stage_b(bool pair, int BN) {
+    return (uint32_t)(pair ? BN / 2 : BN) * kBK * 2;
+}
+static_assert(gemm_stages(true, 128) * (kStageA + gemm_stage_b(true, 128)) == kStages * (kStageA + kStageB),
+              "same ring size");
 
 struct GemmArgs {
     const float* row_scale;  // [M]
@@ -75,14 +85,17 @@ struct GemmSmem {
     uint32_t abort_flag;
 };
 
-template <bool WRITE_I32, bool PAIR, typename T>
+template <bool WRITE_I32, bool PAIR, typename T, int BN = kBN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
               const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_wo, GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int S = PAIR ? kPairStages : kStages;
-    constexpr uint32_t SB = PAIR ? kPairStageB : kStageB;  // B bytes of a stage in this CTA
+    static_assert(BN == kBN || (PAIR && BN == 128), "tile widths: 256, or 128 for CTA pairs");
+    constexpr int S = gemm_stages(PAIR, BN);
+    constexpr uint32_t SB = gemm_stage_b(PAIR, BN);  // B bytes of a stage in this CTA
+    constexpr uint32_t TC = 2 * BN;                  // TMEM columns: two fp32 accumulators
+    constexpr int HC = BN / 2;                       // columns drained by one epilogue warp
     uint8_t* stage_a = smem;
     uint8_t* stage_b = smem + S * kStageA;
     GemmSmem* ss = reinterpret_cast<GemmSmem*>(smem + S * (kStageA + SB));
@@ -92,13 +105,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // work units: 128 x 256 tiles, or 256 x 256 tiles of a CTA pair
     const uint32_t rank = PAIR ? cluster_cta_rank() : 0u;
     const int unit_rows = PAIR ? 2 * kBM : kBM;
-    const int tiles_m = (a.M + unit_rows - 1) / unit_rows, tiles_n = (a.N + kBN - 1) / kBN;
+    const int tiles_m = (a.M + unit_rows - 1) / unit_rows, tiles_n = (a.N + BN - 1) / BN;
     const int ntiles = tiles_m * tiles_n;
     const int unit0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
     const int ustride = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
     // this CTA's first row in unit row tm and first column of its B half
     auto row_of = [&](int tm) { return tm * unit_rows + (int)rank * kBM; };
-    auto bcol_of = [&](int tn) { return tn * kBN + (int)rank * (kBN / 2); };
+    auto bcol_of = [&](int tn) { return tn * BN + (int)rank * (BN / 2); };
     const int ksteps = (a.K + kBK - 1) / kBK;
     const int nchunks_int = (ksteps + kChunkSteps - 1) / kChunkSteps;
 
@@ -126,10 +139,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (warp == 1) {
         if constexpr (PAIR) {
-            tmem_alloc_pair(&ss->tmem_base, kTmemCols);
+            tmem_alloc_pair(&ss->tmem_base, TC);
             tmem_relinquish_pair();
         } else {
-            tmem_alloc(&ss->tmem_base, kTmemCols);
+            tmem_alloc(&ss->tmem_base, TC);
             tmem_relinquish();
         }
     }
@@ -195,7 +208,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     } else {
                         mbar_arrive_expect_tx(&ss->full[stage], kStageA + SB);
                         tma_load_2d(stage_a + stage * kStageA, ta, &ss->full[stage], kx, tm * kBM);
-                        tma_load_2d(stage_b + stage * SB, tb, &ss->full[stage], kx, tn * kBN);
+                        tma_load_2d(stage_b + stage * SB, tb, &ss->full[stage], kx, tn * BN);
                     }
                     issued[stage] = true;
                     issued_parity[stage] = phase;
@@ -214,9 +227,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         // (pairs: the first CTA's thread issues for both)
         if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc = make_idesc_f16(PAIR ? 2 * kBM : kBM, kBN);
+            constexpr uint32_t idesc = make_idesc_f16(PAIR ? 2 * kBM : kBM, BN);
             // the outlier chunk multiplies the gathered X and W values, of format T
-            constexpr uint32_t idesc_o = make_idesc_f16(PAIR ? 2 * kBM : kBM, kBN, Fmt<T>::kBF16);
+            constexpr uint32_t idesc_o = make_idesc_f16(PAIR ? 2 * kBM : kBM, BN, Fmt<T>::kBF16);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t chunk = 0;
@@ -233,7 +246,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const int s_begin = ch < nchunks_int ? ch * kChunkSteps : ksteps;
                     const int s_end = ch < nchunks_int ? min(ksteps, s_begin + kChunkSteps) : ksteps + osteps;
-                    const uint32_t d_tmem = tmem_base + b * (uint32_t)kBN;
+                    const uint32_t d_tmem = tmem_base + b * (uint32_t)BN;
                     const uint32_t id = ch < nchunks_int ? idesc : idesc_o;
                     for (int s = s_begin; s < s_end; ++s) {
                         if (!wait_bar(&ss->full[stage], phase)) {
@@ -292,10 +305,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int tile = unit0; tile < ntiles && ok; tile += ustride) {
             const int tm = tile % tiles_m, tn = tile / tiles_m;
             const int row = row_of(tm) + q * 32 + lane;
-            const int col0 = tn * kBN + h * 128;
-            int32_t sum[128];
+            const int col0 = tn * BN + h * HC;
+            int32_t sum[HC];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) sum[c] = 0;
+            for (int c = 0; c < HC; ++c) sum[c] = 0;
             for (int ch = 0; ch < nchunks_int; ++ch, ++chunk) {
                 const uint32_t b = chunk & 1u, use = (chunk >> 1) & 1u;
                 const bool got = warp_wait(&ss->tmem_full[b], use);
@@ -306,9 +319,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < HC / 16; ++j) {
                     uint32_t r[16];
-                    tmem_ld_32x32b_x16(tmem_base + lane_base + b * kBN + h * 128 + j * 16, r);
+                    tmem_ld_32x32b_x16(tmem_base + lane_base + b * BN + h * HC + j * 16, r);
                     tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 16; ++c) sum[j * 16 + c] += __float2int_rn(__uint_as_float(r[c]));
@@ -333,10 +346,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const bool row_ok = row < a.M;
             const float sx = row_ok ? __ldcg(a.row_scale + row) * (1.0f / 16129.0f) : 0.0f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < HC / 16; ++j) {
                 uint32_t r[16];
                 if (has_f) {
-                    tmem_ld_32x32b_x16(tmem_base + lane_base + fb * kBN + h * 128 + j * 16, r);
+                    tmem_ld_32x32b_x16(tmem_base + lane_base + fb * BN + h * HC + j * 16, r);
                     tmem_ld_wait();
                 } else {
 #pragma unroll
@@ -394,9 +407,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 1) {
         __syncwarp();
         if constexpr (PAIR)
-            tmem_dealloc_pair(tmem_base, kTmemCols);
+            tmem_dealloc_pair(tmem_base, TC);
         else
-            tmem_dealloc(tmem_base, kTmemCols);
+            tmem_dealloc(tmem_base, TC);
     }
 }
 
