@@ -723,11 +723,10 @@ llmint8_status llmint8_selftest_timeout(void* workspace, int spin_limit, void* s
 // Allocation-free entry point.
 //
 // Some callers cannot allocate device memory at the moment they run the matmul:
-// code that executes while a stream is being captured into a CUDA graph (an
-// allocation there is an illegal call that invalidates the capture), callers
-// that must not risk the device-wide synchronization that cudaMalloc/cudaFree
-// may cause inside a latency-critical decode loop, and hosts whose device
-// memory budget is owned by another allocator.  For them the scratch space the
+// callers that must not risk the device-wide synchronization that
+// cudaMalloc/cudaFree may cause inside a latency-critical decode loop, hosts
+// whose device memory budget is owned by another allocator, and plug-ins that
+// are handed device pointers but no allocation rights.  For them the scratch space the
 // matmul needs lives in this file-scope array, sized once at load time; every
 // GPU that loads the library holds it until the process exits.
 // ----------------------------------------------------------------------------

@@ -208,10 +208,10 @@ llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold,
 /*
  * Allocation-free variant of llmint8_matmul.  The pages describe no such call;
  * it exists for callers that cannot allocate device memory when they run the
- * matmul: code running while a stream is captured into a CUDA graph (an
- * allocation there invalidates the capture), latency-critical loops that must
- * not risk the device-wide synchronization of cudaMalloc/cudaFree, and hosts
- * whose device memory is owned by another allocator.
+ * matmul: latency-critical loops that must not risk the device-wide
+ * synchronization of cudaMalloc/cudaFree, hosts whose device memory is owned by
+ * another allocator (a framework's caching pool, an embedding runtime), and
+ * plug-ins that are handed device pointers but no allocation rights.
  *
  * Same arguments and results as llmint8_matmul minus the workspace: the scratch
  * space is a static 8 MiB device array inside the library (held by every GPU

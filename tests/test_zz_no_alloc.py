@@ -2,10 +2,10 @@
 as llmint8_matmul.
 
 It serves callers that cannot allocate device memory when they run the matmul
-(for instance code running during CUDA-graph stream capture, where an
-allocation is illegal, or latency-critical loops that must not risk the
-synchronization of cudaMalloc/cudaFree): its scratch space is a static device
-array inside the library instead of a caller workspace.  Two calls in a row
+(latency-critical loops that must not risk the synchronization of
+cudaMalloc/cudaFree, or hosts whose device memory belongs to another
+allocator): its scratch space is a static device array inside the library
+instead of a caller workspace.  Two calls in a row
 check that the second call is not disturbed by what the first one left in the
 shared array.  This file is collected last on purpose.
 """
