@@ -417,6 +417,9 @@ def run_ours(args, world, rank, local):
     prefill = None
     if not args.no_prefill:
         prefill = run_prefill(args, dev, stream, bf16_peak, peak_src)
+    chain = None
+    if not args.no_chain:
+        chain = run_chain(args, dev, stream)
 
     line = None
     if rank == 0:
@@ -456,6 +459,8 @@ def run_ours(args, world, rank, local):
         }
         if prefill is not None:
             line["prefill"] = prefill
+        if chain is not None:
+            line["chain"] = chain
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -527,6 +532,85 @@ def run_prefill(args, dev, stream, bf16_peak, peak_src, iters=None):
                          "peak_source": f"{peak_src} bf16_tflops (cuBLAS, burst); tcgen05 kind::f16 runs at the "
                                         "bf16 rate; sm_103a has no int8 tcgen05 kind"},
             "shapes": out}
+
+
+def run_chain(args, dev, stream, steps=None):
+    """Decode chain: the three 7B-like layers (4096, 4096) -> (4096, 11008) -> (11008, 4096), each
+    output the next input, for M = 1 and 4.  One step = the 3 calls as one captured graph, weights in
+    rotating replicas; the chained calls (llmint8_matmul_chain: one kernel per layer after the
+    first) against the same flow through llmint8_matmul (X pass + GEMV per layer)."""
+    import torch
+    from bit_quantization_matmul_row_b300 import api
+    steps = steps or max(20, min(200, args.steps))
+    R = args.replicas
+    cases = {(c.M, c.K, c.N): c for c in synthetic.decode_7b()}
+    layers = [(4096, 4096), (4096, 11008), (11008, 4096)]
+    wts = []
+    for K, N in layers:
+        W, _ = cases[(1, K, N)].w()
+        Wd = torch.from_numpy(W).to(dev)
+        Wq, sw, _ = api.llmint8_quantize_weight(Wd, fp16_codes=False)
+        wts.append([(Wq, sw, Wd)] + [(Wq.clone(), sw.clone(), Wd.clone()) for _ in range(R - 1)])
+    out = {}
+    for M in (1, 4):
+        c0 = cases[(M, 4096, 4096)]
+        X0 = torch.from_numpy(c0.x()[0]).to(dev)
+        t = c0.threshold
+        Ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _, N in layers]
+        states = [api.make_chain_state(M, N, dev) for _, N in layers]
+        wss = [api.make_workspace(M, K, N, dev) for K, N in layers]
+
+        def chained(r):
+            x, s_in = X0, None
+            for li in range(len(layers)):
+                Wq, sw, Wd = wts[li][r % R]
+                api.llmint8_matmul_chain(x, t, s_in, Wq, sw, Wd, next_threshold=t, state_out=states[li], Y=Ys[li],
+                                         workspace=wss[li])
+                x, s_in = Ys[li], states[li]
+
+        def separate(r):
+            x = X0
+            for li in range(len(layers)):
+                Wq, sw, Wd = wts[li][r % R]
+                api.llmint8_matmul(x, t, Wq, sw, None, Wd, Y=Ys[li], workspace=wss[li])
+                x = Ys[li]
+
+        res = {}
+        for name, fn in (("separate", separate), ("chained", chained)):
+            fn(0)
+            torch.cuda.synchronize()
+            graphs = []
+            for r in range(R):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn(r)
+                graphs.append(g)
+            for i in range(3 * R):
+                graphs[i % R].replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for i in range(steps):
+                graphs[i % R].replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res[name] = e0.elapsed_time(e1) / steps * 1e3  # us per step
+            del graphs
+        # algorithmic bytes of the step, with the outlier counts the separate flow found
+        separate(0)
+        torch.cuda.synchronize()
+        nbytes = 0
+        for li, (K, N) in enumerate(layers):
+            n_o = api.read_intermediates(wss[li], M, K, N)["outlier_count"]
+            nbytes += alg_bytes(M, K, N, n_o)
+        out[f"M{M}"] = {"chained_us": res["chained"], "separate_us": res["separate"],
+                        "chained_gbs": nbytes / (res["chained"] * 1e-6) / 1e9,
+                        "separate_gbs": nbytes / (res["separate"] * 1e-6) / 1e9,
+                        "speedup": res["separate"] / res["chained"], "bytes_per_step": nbytes}
+    return {"workload": "7B-like decode chain: (4096,4096) -> (4096,11008) -> (11008,4096), each Y the next X; "
+                        "M in {1, 4}; t=6.0 for every layer",
+            "steps": steps, "unit": "GB/s", "timing": "events around replays of one captured graph per step",
+            "results": out}
 
 
 def run_ablation(args):
@@ -627,6 +711,7 @@ def main():
     ap.add_argument("--replicas", type=int, default=4)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-chain", action="store_true")
     ap.add_argument("--max-graphs", type=int, default=256)
     ap.add_argument("--ablation", action="store_true",
                     help="error vs speed: LLM.int8() against plain int8 and the fp16 matmul (one JSON line)")

@@ -27,6 +27,9 @@ EXPORTS = (
     "llmint8_matmul_i32",
     "llmint8_xpass",
     "llmint8_gemm",
+    "llmint8_chain_state_bytes",
+    "llmint8_chain_state_layout",
+    "llmint8_matmul_chain",
     "llmint8_matmul_noalloc",
     "llmint8_kernels_per_call",
     "llmint8_workspace_layout",
@@ -68,6 +71,10 @@ def load() -> ctypes.CDLL:
         lib.llmint8_xpass.argtypes = [P, I, I, I, F, P, Z, P]
         lib.llmint8_gemm.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_noalloc.argtypes = [P, I, I, I, F, P, P, P, P, P, P]
+        lib.llmint8_chain_state_bytes.argtypes = [I, I]
+        lib.llmint8_chain_state_bytes.restype = Z
+        lib.llmint8_chain_state_layout.argtypes = [I, I, ctypes.POINTER(Z)]
+        lib.llmint8_matmul_chain.argtypes = [P, I, I, I, F, P, P, P, P, P, F, P, P, Z, P]
         lib.llmint8_kernels_per_call.argtypes = [I, I, I, F, I]
         lib.llmint8_kernels_per_call.restype = I
         lib.llmint8_workspace_layout.argtypes = [I, I, I, ctypes.POINTER(Z)]
@@ -76,7 +83,8 @@ def load() -> ctypes.CDLL:
         for f in ("llmint8_quantize_weight", "llmint8_matmul", "llmint8_matmul_int8", "llmint8_matmul_i32",
                   "llmint8_matmul_w8", "llmint8_pack_w16_rows", "llmint8_quantize_weight_bf16",
                   "llmint8_matmul_bf16", "llmint8_matmul_i32_bf16",
-                  "llmint8_xpass", "llmint8_gemm", "llmint8_matmul_noalloc", "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
+                  "llmint8_xpass", "llmint8_gemm", "llmint8_matmul_noalloc", "llmint8_chain_state_layout",
+                  "llmint8_matmul_chain", "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
             getattr(lib, f).restype = I
         _lib = lib
         return lib

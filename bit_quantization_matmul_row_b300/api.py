@@ -139,6 +139,39 @@ def llmint8_matmul(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspace=Non
     return Y
 
 
+def llmint8_chain_state_layout(M: int, N: int):
+    """(flags offset, partial-maxima offset, total bytes) of a chain state for an activation [M, N]."""
+    off = (ctypes.c_size_t * 3)()
+    _check(_lib.load().llmint8_chain_state_layout(M, N, off), "llmint8_chain_state_layout")
+    return int(off[0]), int(off[1]), int(off[2])
+
+
+def make_chain_state(M: int, N: int, device=None) -> torch.Tensor:
+    n = _lib.load().llmint8_chain_state_bytes(M, N)
+    if n == 0:
+        raise ValueError(f"no chain state for M={M} N={N}")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def llmint8_matmul_chain(X, threshold, state_in, Wq, colScaleW, W16, next_threshold=6.0, state_out=None, Y=None,
+                         workspace=None, stream=None):
+    """Decode-chain matmul (M <= 4): Y = X.W as llmint8_matmul; with `state_in` (the chain
+    state of X from the previous call) no X pass runs; with `state_out` the chain state of Y
+    for `next_threshold` is written."""
+    M, K, N = _shapes(X, Wq)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    if workspace is None:
+        workspace = make_workspace(M, K, N, X.device)
+    _need(X, torch.float16, (M, K), "X")
+    _need(Y, torch.float16, (M, N), "Y")
+    st = _lib.load().llmint8_matmul_chain(_ptr(X), M, K, N, float(threshold), _ptr(state_in), _ptr(Wq),
+                                          _ptr(colScaleW), _ptr(W16), _ptr(Y), float(next_threshold),
+                                          _ptr(state_out), _ptr(workspace), workspace.numel(), _stream(stream, X))
+    _check(st, "llmint8_matmul_chain")
+    return Y
+
+
 def llmint8_pack_w16_rows(W16, rows, stream=None):
     """Kept fp16 rows of W for llmint8_matmul_w8: (W16c [R, N], row_map int32 [K])."""
     K, N = W16.shape

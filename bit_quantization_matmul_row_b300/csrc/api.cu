@@ -17,6 +17,7 @@
 #include "wquant.cuh"
 #include "gemv.cuh"
 #include "gemm_tc.cuh"
+#include "chain.cuh"
 
 using namespace llmint8;
 
@@ -32,6 +33,7 @@ struct DeviceInfo {
     bool gemm_attr_set[2] = {false, false};
     bool gemv_attr_set[2] = {false, false};
     bool rowq_cluster_attr_set[2] = {false, false};
+    bool chain_attr_set = false;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -79,6 +81,19 @@ llmint8_status encode_fp16_2d(CUtensorMap* map, const void* base, int rows, int 
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? LLMINT8_OK : LLMINT8_ECUDA;
+}
+
+// 2D int8 tensor [rows, cols] row-major (pitch = cols bytes); box of box_rows x
+// box_cols bytes, no swizzle (rows land box_cols bytes apart in shared memory).
+llmint8_status encode_u8_2d(CUtensorMap* map, const void* base, int rows, int cols, int box_rows, int box_cols) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? LLMINT8_OK : LLMINT8_ECUDA;
 }
@@ -518,6 +533,64 @@ llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, 
                                s, gw, src);
 }
 
+// ---- decode chain (chain.cuh): the streaming GEMV for up to 4 rows of X ----
+constexpr size_t kMaxDynSmem = 232448;  // 227 KB, the opt-in limit of one CTA
+constexpr size_t kSmemPerSM = 233472;   // 228 KB, of which 1 KB per resident CTA is reserved
+
+// the kernel's static shared memory (under 1 KB) counts against the same limit
+constexpr size_t kChainMaxDynSmem = kMaxDynSmem - 1024;
+
+bool chain_shape_ok(int M, int K) {
+    return M >= 1 && M <= kChainMaxM && K >= kChainStageK && chain_smem(M, K) <= kChainMaxDynSmem;
+}
+
+template <int MR>
+bool set_chain_attrs() {
+    const int m = (int)kChainMaxDynSmem;
+    const auto a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    return cudaFuncSetAttribute(k_gemv_chain<MR, false, false>, a, m) == cudaSuccess &&
+           cudaFuncSetAttribute(k_gemv_chain<MR, false, true>, a, m) == cudaSuccess &&
+           cudaFuncSetAttribute(k_gemv_chain<MR, true, false>, a, m) == cudaSuccess &&
+           cudaFuncSetAttribute(k_gemv_chain<MR, true, true>, a, m) == cudaSuccess;
+}
+
+template <int MR>
+llmint8_status chain_launch_m(const CUtensorMap& tw, const GemvArgs& ga, const ChainArgs& ch, dim3 grid,
+                              size_t smem, cudaStream_t s) {
+    const dim3 block(kChainThreads);
+    if (ch.in != nullptr)
+        return ch.out != nullptr ? launch(k_gemv_chain<MR, true, true>, grid, block, smem, s, true, tw, ga, ch)
+                                 : launch(k_gemv_chain<MR, true, false>, grid, block, smem, s, true, tw, ga, ch);
+    return ch.out != nullptr ? launch(k_gemv_chain<MR, false, true>, grid, block, smem, s, true, tw, ga, ch)
+                             : launch(k_gemv_chain<MR, false, false>, grid, block, smem, s, true, tw, ga, ch);
+}
+
+// One launch of k_gemv_chain: a persistent grid of up to two CTAs per SM.
+llmint8_status chain_launch(const GemvArgs& ga, const ChainArgs& ch, DeviceInfo* dev, cudaStream_t s) {
+    llmint8_status st;
+    if ((st = get_encoder()) != LLMINT8_OK) return st;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!dev->chain_attr_set) {
+            if (!set_chain_attrs<1>() || !set_chain_attrs<2>() || !set_chain_attrs<3>() || !set_chain_attrs<4>())
+                return LLMINT8_ECUDA;
+            dev->chain_attr_set = true;
+        }
+    }
+    CUtensorMap tw;
+    if ((st = encode_u8_2d(&tw, ga.Wq, ga.N, ga.K, kChainCols, kChainBoxK)) != LLMINT8_OK) return st;
+    const size_t smem = chain_smem(ga.M, ga.K);
+    const int per_sm = 2 * (smem + 1024) <= kSmemPerSM ? 2 : 1;
+    const int strips = ga.N / kChainCols;
+    const dim3 grid(strips < per_sm * dev->sms ? strips : per_sm * dev->sms);
+    switch (ga.M) {
+        case 1: return chain_launch_m<1>(tw, ga, ch, grid, smem, s);
+        case 2: return chain_launch_m<2>(tw, ga, ch, grid, smem, s);
+        case 3: return chain_launch_m<3>(tw, ga, ch, grid, smem, s);
+        default: return chain_launch_m<4>(tw, ga, ch, grid, smem, s);
+    }
+}
+
 // Waits on a barrier nothing completes, bounded by spin_limit polls, then
 // records the timeout in the error word.
 __global__ void k_selftest_timeout(WsHeader* hdr, uint32_t spin_limit) {
@@ -705,6 +778,73 @@ llmint8_status llmint8_device_status(void* workspace, void* stream) {
     if (cudaMemcpy(&word, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return LLMINT8_ECUDA;
     if (word != 0 && cudaMemset(workspace, 0, 4) != cudaSuccess) return LLMINT8_ECUDA;
     return static_cast<llmint8_status>(word);
+}
+
+size_t llmint8_chain_state_bytes(int M, int N) {
+    if (M < 1 || M > kChainMaxM || N < 16 || N > (1 << 30) || (N % 16)) return 0;
+    return chain_state_bytes(M, N);
+}
+
+llmint8_status llmint8_chain_state_layout(int M, int N, size_t* offsets) {
+    if (!offsets || llmint8_chain_state_bytes(M, N) == 0) return LLMINT8_EINVAL;
+    offsets[0] = chain_flags_off();
+    offsets[1] = chain_parts_off(N);
+    offsets[2] = chain_state_bytes(M, N);
+    return LLMINT8_OK;
+}
+
+llmint8_status llmint8_matmul_chain(const void* X, int M, int K, int N, float threshold, const void* state_in,
+                                    const int8_t* Wq, const float* colScaleW, const void* W16, void* Y,
+                                    float next_threshold, void* state_out, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+    Layout L;
+    DeviceInfo* dev = nullptr;
+    // with a state in, its flags stand for the threshold (the argument is not used)
+    const float t = state_in ? 0.0f : threshold;
+    llmint8_status st = check_common(X, M, K, N, t, workspace, workspace_bytes, &L, &dev);
+    if (st != LLMINT8_OK) return st;
+    if (!Wq || !colScaleW || !Y) return LLMINT8_EINVAL;
+    if (state_out && std::isnan(next_threshold)) return LLMINT8_EINVAL;
+    if (state_in && state_in == state_out) return LLMINT8_EINVAL;
+    const bool use_outliers = !(std::isinf(t) && t > 0);
+    if (use_outliers && !W16) return LLMINT8_EINVAL;
+    if (!aligned16(Wq) || !aligned16(colScaleW) || !aligned16(Y) || (W16 && !aligned16(W16)) ||
+        (state_in && !aligned16(state_in)) || (state_out && !aligned16(state_out)))
+        return LLMINT8_EALIGN;
+    if (!chain_shape_ok(M, K)) return LLMINT8_EUNSUPPORTED;
+    if ((st = current_device(&dev)) != LLMINT8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!state_in && (st = xpass_launch<__half>(X, M, K, threshold, workspace, L, dev, s, W16, N, false)) != LLMINT8_OK)
+        return st;
+    const WsView w(workspace, L);
+    GemvArgs ga;
+    ga.codes = reinterpret_cast<const int8_t*>(w.codes);
+    ga.Wq = Wq;
+    ga.col_scale = colScaleW;
+    ga.row_scale = w.row_scale;
+    ga.W16 = static_cast<const __half*>(W16);
+    ga.hdr = w.hdr;
+    ga.outlier_idx = w.idx;
+    ga.xo = w.xo;
+    ga.xo_pitch = L.kp;
+    ga.out = Y;
+    ga.M = M;
+    ga.K = K;
+    ga.N = N;
+    ga.k_per_warp = 0;
+    ga.use_outliers = use_outliers ? 1 : 0;
+    ga.w8 = 0;
+    ga.W16c = nullptr;
+    ga.row_map = nullptr;
+    ga.w16_rows = 0;
+    ChainArgs ch;
+    ch.X = static_cast<const __half*>(X);
+    ch.in = static_cast<const uint8_t*>(state_in);
+    ch.out = static_cast<uint8_t*>(state_out);
+    ch.next_t = next_threshold;
+    ch.err = w.hdr;
+    ch.spin_limit = kDefaultSpinLimit;
+    return chain_launch(ga, ch, dev, s);
 }
 
 llmint8_status llmint8_selftest_timeout(void* workspace, int spin_limit, void* stream) {

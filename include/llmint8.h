@@ -206,6 +206,46 @@ llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold,
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Decode chain (1 <= M <= 4 rows, fp16): a matmul whose GEMV also prepares the
+ * X pass of the next layer, when its output Y is that layer's input.  The
+ * pages place the small-batch cost of the method in the per-forward handling
+ * of the activations (LLM.int8() overview, section 3); here the outlier
+ * columns of Y (A1 for the next threshold, paper walkthrough section 2.1) and
+ * the row absmax of Y over the other columns (A2, section 2.3) are computed in
+ * the GEMV's epilogue and left in a "chain state", so the next call runs one
+ * kernel and no X pass.  Results are those of llmint8_matmul on the same X.
+ *
+ *   X               in   fp16 [M, K] device (the previous layer's Y)
+ *   threshold       in   outlier threshold of X, used only without state_in
+ *   state_in        in   chain state of X written by the previous call's
+ *                        state_out (same M, N of that call = K here), or NULL:
+ *                        then the usual X pass runs first
+ *   Wq, colScaleW, W16, Y   as llmint8_matmul (no Wq16: the GEMV reads Wq)
+ *   next_threshold  in   threshold the flags of Y are taken for (not NaN)
+ *   state_out       out  chain state of Y (llmint8_chain_state_bytes(M, N)
+ *                        bytes, 16-byte aligned), or NULL
+ *   workspace       scratch as llmint8_matmul (error word, X-pass results)
+ *
+ * Chain state layout (llmint8_chain_state_layout): a 256-byte header (int32 M,
+ * N, nparts, float threshold), then uint8 flags [N] (1 = outlier column), then
+ * float [nparts][M] partial row maxima (the row scale is their maximum).  A
+ * caller may fill one by hand with nparts = 1.
+ *
+ * Errors as llmint8_matmul; EUNSUPPORTED for M > 4, K < 512, or M * K too
+ * large for shared memory; EINVAL if state_in == state_out, W16 is NULL while
+ * outliers are possible, or next_threshold is NaN with a state_out; EALIGN for
+ * a state pointer that is not 16-byte aligned.  state_in must not overlap Y or
+ * state_out.  One kernel per call with state_in, else the X pass kernels plus
+ * one.  Asynchronous on `stream`.
+ */
+size_t llmint8_chain_state_bytes(int M, int N);
+llmint8_status llmint8_chain_state_layout(int M, int N, size_t *offsets /* [3]: flags, parts, total */);
+llmint8_status llmint8_matmul_chain(const void *X, int M, int K, int N, float threshold, const void *state_in,
+                                    const int8_t *Wq, const float *colScaleW, const void *W16, void *Y,
+                                    float next_threshold, void *state_out, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/*
  * Allocation-free variant of llmint8_matmul.  The pages describe no such call;
  * it exists for callers that cannot allocate device memory when they run the
  * matmul: latency-critical loops that must not risk the device-wide

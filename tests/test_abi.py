@@ -115,6 +115,36 @@ def test_noalloc_argument_errors(lib):
                                       P(FAKE), None) == _lib.EINVAL
 
 
+def _chain(lib, M=1, K=4096, N=4096, t=6.0, sin=0, w16=FAKE, nt=6.0, sout=FAKE + 4096, Y=FAKE, wsb=1 << 40):
+    P = ctypes.c_void_p
+    return lib.llmint8_matmul_chain(P(FAKE), M, K, N, t, P(sin) if sin else None, P(FAKE), P(FAKE),
+                                    P(w16) if w16 else None, P(Y), nt, P(sout) if sout else None, P(FAKE), wsb, None)
+
+
+def test_chain_state_layout(lib):
+    assert lib.llmint8_chain_state_bytes(5, 64) == 0
+    assert lib.llmint8_chain_state_bytes(1, 40) == 0
+    n = lib.llmint8_chain_state_bytes(4, 11008)
+    off = (ctypes.c_size_t * 3)()
+    assert lib.llmint8_chain_state_layout(4, 11008, off) == _lib.OK
+    flags, parts, total = off[0], off[1], off[2]
+    assert flags == 256 and parts >= flags + 11008 and parts % 256 == 0
+    assert total == n == parts + (11008 // 16) * 4 * 4
+    assert lib.llmint8_chain_state_layout(0, 16, off) == _lib.EINVAL
+
+
+def test_chain_argument_errors(lib):
+    assert _chain(lib, M=5) == _lib.EUNSUPPORTED        # more than 4 rows
+    assert _chain(lib, K=256) == _lib.EUNSUPPORTED      # shorter than one 512-wide ring stage
+    assert _chain(lib, M=4, K=65536) == _lib.EUNSUPPORTED  # codes do not fit in shared memory
+    assert _chain(lib, sin=FAKE + 4096) == _lib.EINVAL  # state in == state out
+    assert _chain(lib, nt=math.nan) == _lib.EINVAL
+    assert _chain(lib, w16=0) == _lib.EINVAL            # outliers possible, no fp16 weight
+    assert _chain(lib, sin=FAKE + 8) == _lib.EALIGN
+    assert _chain(lib, t=math.nan) == _lib.EINVAL
+    assert _chain(lib, wsb=16) == _lib.EWORKSPACE
+
+
 def test_selftest_argument_errors(lib):
     P = ctypes.c_void_p
     assert lib.llmint8_selftest_timeout(P(0), 10, None) == _lib.EINVAL
