@@ -130,6 +130,22 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(ms, world, device=None):
+    """The slowest rank's time: a job of independent replicas ends when its last rank does."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank_step, steps, world, ms):
+    """Whole-job throughput in units per second: what all ranks processed over the slowest rank's time."""
+    return units_per_rank_step * steps * world / (ms * 1e-3)
+
+
 # ---------------------------------------------------------------------------- CPU oracle
 
 def cpu_oracle_time(cases_xw, n_sample_cols=None, min_seconds=10.0, max_reps=8):
@@ -340,12 +356,9 @@ def run_ours(args, world, rank, local):
     st = api.llmint8_device_status(cases[0]["ws"])
     if st != 0:
         raise SystemExit(f"device error word {st}")
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     total_bytes = step_bytes * args.steps * world
-    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+    value = job_rate(step_bytes, args.steps, world, elapsed_ms) / 1e9
     per_shape = [{"M": d["c"].M, "K": d["c"].K, "N": d["c"].N, "outliers": d["n_o"], "kernel": d["form"],
                   "kernel_us": 1e3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G,
                   "kernel_gbs": d["bytes"] / (1e-3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G) / 1e9}
@@ -391,12 +404,7 @@ def run_ours(args, world, rank, local):
             fn(i)
         ev_b.record()
         torch.cuda.synchronize()
-        ms = ev_a.elapsed_time(ev_b)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(ev_a.elapsed_time(ev_b), world, dev)
 
     e2e_ms = timed(e2e_step, args.steps)
     e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
