@@ -54,6 +54,7 @@ constexpr int kChainBox = kChainCols * kChainBoxK;       // 4 KB
 constexpr int kChainStage = 2 * kChainBox;               // 8 KB
 constexpr int kChainStages = 8;
 constexpr int kChainPre = 2;             // outlier positions per lane held in registers
+constexpr int kChainBatch = 4;           // outlier positions per lane loaded together past those
 constexpr uint32_t kChainBulk = 32768;   // bytes per bulk copy of the X codes
 
 // Chain state of an activation [M, N] (device memory):
@@ -430,12 +431,37 @@ __global__ void __launch_bounds__(kChainThreads, 2)
                     f1 = fmaf(xv, w1, f1);
                 }
             }
-            for (int jo = oj + LPR * kChainPre; jo < cnt; jo += LPR) {  // past the registers: through L2
-                if (orow) {
-                    const int k = outlier_col(jo);
-                    const float xv = __half2float(__ushort_as_half((unsigned short)outlier_x(oi, jo, k)));
-                    f0 = fmaf(xv, w16_value<__half>(a, k, nA), f0);
-                    f1 = fmaf(xv, w16_value<__half>(a, k, nA + 1), f1);
+            // past the registers: through L2, kChainBatch positions per round so that
+            // their loads are in flight together (same summation order as one by one)
+            for (int jb = oj + LPR * kChainPre; jb < cnt; jb += kChainBatch * LPR) {
+                if (!orow) continue;
+                int kb[kChainBatch];
+                uint32_t xb[kChainBatch], wb[kChainBatch];
+#pragma unroll
+                for (int u = 0; u < kChainBatch; ++u) {
+                    const int jo = jb + u * LPR;
+                    kb[u] = jo < cnt ? outlier_col(jo) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < kChainBatch; ++u) {
+                    const int jo = jb + u * LPR;
+                    xb[u] = jo < cnt ? outlier_x(oi, jo, kb[u]) : 0u;
+                    wb[u] = (jo < cnt && !a.w8) ? chain_ldg_nc_u32(a.W16 + (size_t)kb[u] * N + nA) : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < kChainBatch; ++u) {
+                    if (jb + u * LPR >= cnt) break;
+                    const float xv = __half2float(__ushort_as_half((unsigned short)xb[u]));
+                    float w0, w1;
+                    if (!a.w8) {
+                        w0 = __half2float(__ushort_as_half((unsigned short)(wb[u] & 0xffffu)));
+                        w1 = __half2float(__ushort_as_half((unsigned short)(wb[u] >> 16)));
+                    } else {
+                        w0 = w16_value<__half>(a, kb[u], nA);
+                        w1 = w16_value<__half>(a, kb[u], nA + 1);
+                    }
+                    f0 = fmaf(xv, w0, f0);
+                    f1 = fmaf(xv, w1, f1);
                 }
             }
 #pragma unroll
