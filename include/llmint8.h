@@ -227,9 +227,10 @@ llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold,
  *   workspace       scratch as llmint8_matmul (error word, X-pass results)
  *
  * Chain state layout (llmint8_chain_state_layout): a 256-byte header (int32 M,
- * N, nparts, float threshold), then uint8 flags [N] (1 = outlier column), then
- * float [nparts][M] partial row maxima (the row scale is their maximum).  A
- * caller may fill one by hand with nparts = 1.
+ * N, nparts, float threshold), then uint8 flags [N] (1 = outlier column, 0 =
+ * not; no other values), then float [nparts][M] partial row maxima (the row
+ * scale is their maximum; non-negative).  A caller may fill one by hand with
+ * nparts = 1; M and N in the header must match the call that reads it.
  *
  * Errors as llmint8_matmul; EUNSUPPORTED for M > 4, K < 512, or M * K too
  * large for shared memory; EINVAL if state_in == state_out, W16 is NULL while
