@@ -219,7 +219,7 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------------------- our arm
 
 KERNEL_SOURCES = {  # the sources each timed kernel is compiled from
-    "k_gemv_decode": ("gemv.cuh", "common.cuh"),
+    "k_gemv_stream": ("gemv_stream.cuh", "gemv.cuh", "common.cuh"),
 }
 
 
@@ -291,10 +291,7 @@ def run_ours(args, world, rank, local):
     for d in cases:
         c = d["c"]
         d["kpc"] = api.llmint8_kernels_per_call(c.M, c.K, c.N, c.threshold)
-        # one GEMV family (same sources): one-tile CTAs, or the persistent form when
-        # up to 8 rows meet more 16-column tiles than two CTAs per SM
-        d["kernel"] = "k_gemv_decode"
-        d["form"] = "k_gemv_decode_tiles" if c.M <= 8 and c.N // 16 > 2 * sms else "k_gemv_decode"
+        d["kernel"] = "k_gemv_stream"  # the decode GEMV: one persistent CTA per SM
     launches_per_step = sum(d["kpc"] for d in cases)
 
     # ---- one CUDA graph per step (the 9 llmint8_matmul calls), so the GPU is not
@@ -353,29 +350,53 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     gemv_ms = [[e0.elapsed_time(e1) for (e0, e1) in igraphs[gi][1]] for gi in range(G)]
     del igraphs
+    # ... and back to back: per shape, one captured graph of B consecutive
+    # llmint8_gemm calls (A3-A5) on a workspace its X pass filled beforehand,
+    # weights rotating through the replicas; consecutive GEMVs overlap through
+    # programmatic dependent launch as they do inside a step.  Events around the
+    # replays; per launch = elapsed / launches.
+    B, GR = 4 * R, 8
+    b2b_us = []
+    for d in cases:
+        c = d["c"]
+        api.llmint8_xpass(d["Xd"], c.threshold, c.N, d["ws"])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for r in range(B):
+                Wq, sw, Wd = d["reps"][r % R]
+                api.llmint8_gemm(d["Xd"], c.threshold, Wq, sw, None, Wd, d["Y"], d["ws"])
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        ev_a.record(stream)
+        for _ in range(GR):
+            g.replay()
+        ev_b.record(stream)
+        torch.cuda.synchronize()
+        b2b_us.append(1e3 * ev_a.elapsed_time(ev_b) / (B * GR))
+        del g
     st = api.llmint8_device_status(cases[0]["ws"])
     if st != 0:
         raise SystemExit(f"device error word {st}")
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     total_bytes = step_bytes * args.steps * world
     value = job_rate(step_bytes, args.steps, world, elapsed_ms) / 1e9
-    per_shape = [{"M": d["c"].M, "K": d["c"].K, "N": d["c"].N, "outliers": d["n_o"], "kernel": d["form"],
-                  "kernel_us": 1e3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G,
-                  "kernel_gbs": d["bytes"] / (1e-3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G) / 1e9}
+    iso_us = [1e3 * sum(gemv_ms[gi][ci] for gi in range(G)) / G for ci in range(ncase)]
+    per_shape = [{"M": d["c"].M, "K": d["c"].K, "N": d["c"].N, "outliers": d["n_o"], "kernel": d["kernel"],
+                  "bytes": d["bytes"], "kernel_us": b2b_us[ci], "kernel_gbs": d["bytes"] / (b2b_us[ci] * 1e-6) / 1e9,
+                  "frac": d["bytes"] / (b2b_us[ci] * 1e-6) / 1e9 / hbm_peak,
+                  "isolated_us": iso_us[ci], "isolated_gbs": d["bytes"] / (iso_us[ci] * 1e-6) / 1e9}
                  for ci, d in enumerate(cases)]
-    by_kernel = {}
-    for ci, d in enumerate(cases):
-        k = by_kernel.setdefault(d["kernel"], {"ms": 0.0, "bytes": 0, "launches": 0})
-        k["ms"] += sum(gemv_ms[gi][ci] for gi in range(G))
-        k["bytes"] += d["bytes"] * G
-        k["launches"] += G
-    dom = max(by_kernel, key=lambda k: by_kernel[k]["ms"])
-    all_ms = sum(k["ms"] for k in by_kernel.values())
-    kernels = {k: {"launches_timed": v["launches"], "launch_us_avg": 1e3 * v["ms"] / v["launches"],
-                   "alg_bytes_per_launch": v["bytes"] / v["launches"],
-                   "achieved_gbs": v["bytes"] / (v["ms"] * 1e-3) / 1e9, "time_share": v["ms"] / all_ms}
-               for k, v in by_kernel.items()}
-    achieved = kernels[dom]["achieved_gbs"]
+    dom = "k_gemv_stream"
+    launch_bytes = sum(d["bytes"] for d in cases) / ncase
+    launch_us = sum(b2b_us) / ncase
+    achieved = launch_bytes / (launch_us * 1e-6) / 1e9
+    iso_launch_us = sum(iso_us) / ncase
+    kernels = {dom: {"launches_timed": ncase * B * GR, "launch_us_avg": launch_us,
+                     "alg_bytes_per_launch": launch_bytes, "achieved_gbs": achieved,
+                     "time_share_of_step": ncase * launch_us * 1e-3 / (elapsed_ms / args.steps),
+                     "isolated_launch_us_avg": iso_launch_us,
+                     "isolated_achieved_gbs": launch_bytes / (iso_launch_us * 1e-6) / 1e9}}
     time.sleep(0.1)
 
     # ---- end to end through the public call: pinned host X -> device,
@@ -386,12 +407,11 @@ def run_ours(args, world, rank, local):
     d2h = sum(d["c"].M * d["c"].N * 2 for d in cases)
 
     def e2e_step(i):
+        # the public host-buffer call: X_host -> device, A1..A5, Y -> Y_host, one C call per matmul
         for ci, d in enumerate(cases):
             c = d["c"]
             Wq, sw, Wd = d["reps"][(i * ncase + ci) % R]
-            d["Xd"].copy_(hX[ci], non_blocking=True)
-            api.llmint8_matmul(d["Xd"], c.threshold, Wq, sw, None, Wd, Y=d["Y"], workspace=d["ws"])
-            hY[ci].copy_(d["Y"], non_blocking=True)
+            api.llmint8_matmul_host(hX[ci], d["Xd"], c.threshold, Wq, sw, None, Wd, d["Y"], hY[ci], d["ws"])
 
     def timed(fn, n):
         for i in range(args.warmup):
@@ -428,6 +448,9 @@ def run_ours(args, world, rank, local):
     chain = None
     if not args.no_chain:
         chain = run_chain(args, dev, stream)
+    sweep = None
+    if not args.no_sweep:
+        sweep = run_sweep(args, dev, stream, hbm_peak, bf16_peak, peak_src)
 
     line = None
     if rank == 0:
@@ -453,14 +476,18 @@ def run_ours(args, world, rank, local):
                          "alg_bytes_per_launch": kernels[dom]["alg_bytes_per_launch"],
                          "launch_us_avg": kernels[dom]["launch_us_avg"],
                          "launches_timed": kernels[dom]["launches_timed"],
-                         "timing": "CUDA events around each GEMV launch in captured steps (the GEMV is not "
-                                   "overlapped with its X pass there); the step value runs the same calls without "
-                                   "those events",
+                         "timing": ("CUDA events around replays of one captured graph per decode shape holding "
+                                    f"{B} consecutive llmint8_gemm calls (A3-A5; X pass run once before; weights "
+                                    "rotating through the replicas; PDL between the launches, as inside a step); "
+                                    "per launch = elapsed / launches, averaged over the 9 shapes.  isolated_*: "
+                                    "events around each GEMV launch inside captured steps, which adds the launch "
+                                    "latency (~5 us on this part for an empty kernel) that PDL hides in a step"),
                          "peak_source": f"{peak_src} hbm_gbs (copy, burst)", "kernels": kernels,
                          "per_shape": per_shape},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "mode": "eager: each call issued from Python through the public llmint8_matmul",
+                    "mode": "eager: each call issued from Python through the public llmint8_matmul_host "
+                            "(pinned host X copied in, Y copied out, inside the call)",
                     "graph_value": e2e_graph_value},
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
@@ -469,6 +496,8 @@ def run_ours(args, world, rank, local):
             line["prefill"] = prefill
         if chain is not None:
             line["chain"] = chain
+        if sweep is not None:
+            line["sweep"] = sweep
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -540,6 +569,90 @@ def run_prefill(args, dev, stream, bf16_peak, peak_src, iters=None):
                          "peak_source": f"{peak_src} bf16_tflops (cuBLAS, burst); tcgen05 kind::f16 runs at the "
                                         "bf16 rate; sm_103a has no int8 tcgen05 kind"},
             "shapes": out}
+
+
+def run_sweep(args, dev, stream, hbm_peak, bf16_peak, peak_src):
+    """The larger configurations: the 13B-like FFN (M=4096, (K,N) in {(5120,13824),(13824,5120)}, 1 %
+    outlier columns of absmax U(20,100), 0.5 % of W's columns x10) and the 70B-like sweep (K=8192,
+    N in {8192, 28672}, M in {1,16,256,2048,8192}, outlier fractions 0 / 0.1 / 1 / 5 % of absmax
+    U(20,60), W ~N(0,0.015)), plus, per (M, N), plain int8 (threshold +inf) and the fp16 matmul
+    (cuBLAS through torch.matmul, context).  Each number: CUDA events around n consecutive public
+    calls (after warm-up), weights rotating through replicas so that every call reads them from
+    HBM.  X is drawn once per (M, fraction) and W once per (K, N) (the first case's seed).
+    Metric per row: TOPS = 2MNK / t for M > 16 (against the bf16 peak: sm_103a has no int8 tcgen05
+    kind), GB/s of algorithmic bytes for M <= 16 (against the HBM copy peak)."""
+    import torch
+    from bit_quantization_matmul_row_b300 import api
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, n, warm=3):
+        for i in range(warm):
+            fn(i)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / n  # us per call
+
+    groups = {}
+    for c in synthetic.ffn_13b() + synthetic.sweep_70b():
+        groups.setdefault((c.K, c.N, c.sigma, c.boosted_frac), []).append(c)
+    xcache = {}
+    rows = []
+    for (K, N, _, _), cs in groups.items():
+        W, _ = cs[0].w()
+        Wd = torch.from_numpy(W).to(dev)
+        del W
+        Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd)
+        R2 = max(2, -(-3 * L2_BYTES // (K * N)))  # replicas: >= 3 x L2 of int8 weights between re-reads
+        R2 = min(R2, 4)
+        reps = [(Wq, sw, Wq16, Wd)] + [(Wq.clone(), sw.clone(), Wq16.clone(), Wd.clone()) for _ in range(R2 - 1)]
+        for c in cs:
+            key = (c.M, K, c.frac, c.mag)
+            if key not in xcache:
+                xcache.clear()
+                xcache[key] = torch.from_numpy(c.x()[0]).to(dev)
+            Xd = xcache[key]
+            M = c.M
+            ws = api.make_workspace(M, K, N, dev)
+            Y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            n = 20 if M <= 256 else (10 if M <= 2048 else 5)
+            dec = M <= 16
+
+            def call(i, t=c.threshold):
+                Wq_, sw_, Wq16_, Wd_ = reps[i % R2]
+                api.llmint8_matmul(Xd, t, Wq_, sw_, None if dec else Wq16_, Wd_, Y=Y, workspace=ws, stream=stream)
+
+            us = timed(call, n)
+            n_o = api.read_intermediates(ws, M, K, N)["outlier_count"]
+            flop = 2.0 * M * N * K
+            row = {"case": c.name, "M": M, "K": K, "N": N, "outlier_frac": c.frac, "outliers": n_o, "us": us,
+                   "tops": flop / (us * 1e-6) / 1e12}
+            if dec:
+                gbs = alg_bytes(M, K, N, n_o) / (us * 1e-6) / 1e9
+                row.update(gbs=gbs, bound="hbm", frac=gbs / hbm_peak, kernel="k_gemv_stream")
+            else:
+                row.update(bound="tensor", frac=row["tops"] / bf16_peak, kernel="k_gemm_tc")
+            if c.frac == 0.001 or (c.frac == 0.01 and K != 8192):
+                # per (M, N): plain int8 and the fp16 matmul on the same X
+                row["int8_t_inf_us"] = timed(lambda i: call(i, float("inf")), n)
+                row["fp16_cublas_us"] = timed(lambda i: torch.matmul(Xd, reps[i % R2][3], out=Y), n)
+            rows.append(row)
+            del ws, Y
+        del reps, Wq, sw, Wq16, Wd
+        xcache.clear()
+        torch.cuda.empty_cache()
+    return {"workloads": ["13B-like FFN: M=4096, (K,N) in {(5120,13824),(13824,5120)}; 1% outlier columns "
+                          "U(20,100); W ~N(0,0.02) with 0.5% columns x10; t=6.0",
+                          "70B-like sweep: K=8192, N in {8192,28672}, M in {1,16,256,2048,8192}; outlier "
+                          "fraction in {0, 0.1%, 1%, 5%} U(20,60); W ~N(0,0.015); t=6.0; plus t=+inf and "
+                          "fp16 cuBLAS per (M, N)"],
+            "timing": "CUDA events around n consecutive public llmint8_matmul calls (n = 20 / 10 / 5 for "
+                      "M <= 256 / 2048 / 8192), weights rotating through replicas (inputs larger than L2)",
+            "peaks": {"hbm_gbs": hbm_peak, "bf16_tflops": bf16_peak, "source": peak_src},
+            "rows": rows}
 
 
 def run_chain(args, dev, stream, steps=None):
@@ -739,6 +852,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-chain", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the 13B FFN / 70B sweep shapes")
     ap.add_argument("--max-graphs", type=int, default=256)
     ap.add_argument("--ablation", action="store_true",
                     help="error vs speed: LLM.int8() against plain int8 and the fp16 matmul (one JSON line)")

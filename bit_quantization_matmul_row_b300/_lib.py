@@ -18,6 +18,7 @@ EXPORTS = (
     "llmint8_quantize_weight",
     "llmint8_workspace_bytes",
     "llmint8_matmul",
+    "llmint8_matmul_host",
     "llmint8_matmul_int8",
     "llmint8_matmul_w8",
     "llmint8_pack_w16_rows",
@@ -30,6 +31,9 @@ EXPORTS = (
     "llmint8_chain_state_bytes",
     "llmint8_chain_state_layout",
     "llmint8_matmul_chain",
+    "llmint8_matmul_chain_i32",
+    "llmint8_quantize_x",
+    "llmint8_read_outliers",
     "llmint8_matmul_noalloc",
     "llmint8_kernels_per_call",
     "llmint8_workspace_layout",
@@ -61,6 +65,7 @@ def load() -> ctypes.CDLL:
         lib.llmint8_workspace_bytes.argtypes = [I, I, I]
         lib.llmint8_workspace_bytes.restype = Z
         lib.llmint8_matmul.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
+        lib.llmint8_matmul_host.argtypes = [P, P, I, I, I, F, P, P, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_int8.argtypes = [P, I, I, I, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_w8.argtypes = [P, I, I, I, F, P, P, P, P, P, I, P, P, Z, P]
         lib.llmint8_pack_w16_rows.argtypes = [P, I, I, P, I, P, P, P]
@@ -74,17 +79,21 @@ def load() -> ctypes.CDLL:
         lib.llmint8_chain_state_bytes.argtypes = [I, I]
         lib.llmint8_chain_state_bytes.restype = Z
         lib.llmint8_chain_state_layout.argtypes = [I, I, ctypes.POINTER(Z)]
-        lib.llmint8_matmul_chain.argtypes = [P, I, I, I, F, P, P, P, P, P, F, P, P, Z, P]
+        lib.llmint8_matmul_chain.argtypes = [P, I, I, I, F, P, Z, P, P, P, P, F, P, Z, P, Z, P]
+        lib.llmint8_matmul_chain_i32.argtypes = [P, I, I, I, F, P, Z, P, P, P, P, F, P, Z, P, P, Z, P]
+        lib.llmint8_quantize_x.argtypes = [P, I, I, F, P, P, P, Z, P]
+        lib.llmint8_read_outliers.argtypes = [P, I, ctypes.POINTER(I), P, I, P]
         lib.llmint8_kernels_per_call.argtypes = [I, I, I, F, I]
         lib.llmint8_kernels_per_call.restype = I
         lib.llmint8_workspace_layout.argtypes = [I, I, I, ctypes.POINTER(Z)]
         lib.llmint8_device_status.argtypes = [P, P]
         lib.llmint8_selftest_timeout.argtypes = [P, I, P]
-        for f in ("llmint8_quantize_weight", "llmint8_matmul", "llmint8_matmul_int8", "llmint8_matmul_i32",
+        for f in ("llmint8_quantize_weight", "llmint8_matmul", "llmint8_matmul_host", "llmint8_matmul_int8", "llmint8_matmul_i32",
                   "llmint8_matmul_w8", "llmint8_pack_w16_rows", "llmint8_quantize_weight_bf16",
                   "llmint8_matmul_bf16", "llmint8_matmul_i32_bf16",
                   "llmint8_xpass", "llmint8_gemm", "llmint8_matmul_noalloc", "llmint8_chain_state_layout",
-                  "llmint8_matmul_chain", "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
+                  "llmint8_matmul_chain", "llmint8_matmul_chain_i32", "llmint8_quantize_x",
+                  "llmint8_read_outliers", "llmint8_workspace_layout", "llmint8_device_status", "llmint8_selftest_timeout"):
             getattr(lib, f).restype = I
         _lib = lib
         return lib

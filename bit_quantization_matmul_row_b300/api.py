@@ -139,6 +139,23 @@ def llmint8_matmul(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspace=Non
     return Y
 
 
+def llmint8_matmul_host(X_host, X, threshold, Wq, colScaleW, Wq16, W16, Y, Y_host, workspace, stream=None):
+    """llmint8_matmul between host tensors: X_host -> X (device), Y = X.W, Y -> Y_host, all
+    enqueued on the stream by one call (synchronize before reading Y_host)."""
+    M, K, N = _shapes(X, Wq)
+    _need(X_host, torch.float16, (M, K), "X_host")
+    _need(X, torch.float16, (M, K), "X")
+    _need(Y, torch.float16, (M, N), "Y")
+    _need(Y_host, torch.float16, (M, N), "Y_host")
+    if X_host.is_cuda or Y_host.is_cuda or not X.is_cuda:
+        raise ValueError("llmint8_matmul_host: X_host and Y_host are host tensors, X and Y device tensors")
+    st = _lib.load().llmint8_matmul_host(_ptr(X_host), _ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW),
+                                         _ptr(Wq16), _ptr(W16), _ptr(Y), _ptr(Y_host), _ptr(workspace),
+                                         workspace.numel(), _stream(stream, X))
+    _check(st, "llmint8_matmul_host")
+    return Y_host
+
+
 def llmint8_chain_state_layout(M: int, N: int):
     """(flags offset, partial-maxima offset, total bytes) of a chain state for an activation [M, N]."""
     off = (ctypes.c_size_t * 3)()
@@ -153,11 +170,23 @@ def make_chain_state(M: int, N: int, device=None) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
+def _state(S, M, cols, device, name):
+    """A chain state buffer: uint8 on `device`, at least llmint8_chain_state_bytes(M, cols) bytes."""
+    if S is None:
+        return 0
+    need = int(_lib.load().llmint8_chain_state_bytes(M, cols))
+    if S.dtype != torch.uint8 or S.device != device or not S.is_contiguous() or S.numel() < need:
+        raise ValueError(f"{name}: expected a contiguous uint8 tensor on {device} of at least {need} bytes, "
+                         f"got {S.dtype} {tuple(S.shape)} on {S.device}")
+    return S.numel()
+
+
 def llmint8_matmul_chain(X, threshold, state_in, Wq, colScaleW, W16, next_threshold=6.0, state_out=None, Y=None,
-                         workspace=None, stream=None):
+                         workspace=None, stream=None, C=None):
     """Decode-chain matmul (M <= 4): Y = X.W as llmint8_matmul; with `state_in` (the chain
     state of X from the previous call) no X pass runs; with `state_out` the chain state of Y
-    for `next_threshold` is written."""
+    for `next_threshold` is written.  With `C` (int32 [M, N]) the exact accumulator of the
+    int8 product is written too (llmint8_matmul_chain_i32)."""
     M, K, N = _shapes(X, Wq)
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
@@ -165,11 +194,51 @@ def llmint8_matmul_chain(X, threshold, state_in, Wq, colScaleW, W16, next_thresh
         workspace = make_workspace(M, K, N, X.device)
     _need(X, torch.float16, (M, K), "X")
     _need(Y, torch.float16, (M, N), "Y")
-    st = _lib.load().llmint8_matmul_chain(_ptr(X), M, K, N, float(threshold), _ptr(state_in), _ptr(Wq),
-                                          _ptr(colScaleW), _ptr(W16), _ptr(Y), float(next_threshold),
-                                          _ptr(state_out), _ptr(workspace), workspace.numel(), _stream(stream, X))
+    _need(C, torch.int32, (M, N), "C")
+    nin = _state(state_in, M, K, X.device, "state_in")
+    nout = _state(state_out, M, N, X.device, "state_out")
+    lib = _lib.load()
+    args = (_ptr(X), M, K, N, float(threshold), _ptr(state_in), nin, _ptr(Wq), _ptr(colScaleW), _ptr(W16), _ptr(Y),
+            float(next_threshold), _ptr(state_out), nout)
+    if C is None:
+        st = lib.llmint8_matmul_chain(*args, _ptr(workspace), workspace.numel(), _stream(stream, X))
+    else:
+        st = lib.llmint8_matmul_chain_i32(*args, _ptr(C), _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul_chain")
     return Y
+
+
+def llmint8_quantize_x(X, threshold, Xq=None, rowScaleX=None, workspace=None, stream=None):
+    """A1 + A2 into caller buffers: (Xq int8 [M, K], rowScaleX fp32 [M], workspace holding the outlier set)."""
+    M, K = X.shape
+    dev = X.device
+    if Xq is None:
+        Xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+    if rowScaleX is None:
+        rowScaleX = torch.empty((M,), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = make_workspace(M, K, 16, dev)
+    _need(X, torch.float16, (M, K), "X")
+    _need(Xq, torch.int8, (M, K), "Xq")
+    _need(rowScaleX, torch.float32, (M,), "rowScaleX")
+    st = _lib.load().llmint8_quantize_x(_ptr(X), M, K, float(threshold), _ptr(Xq), _ptr(rowScaleX), _ptr(workspace),
+                                        workspace.numel(), _stream(stream, X))
+    _check(st, "llmint8_quantize_x")
+    return Xq, rowScaleX, workspace
+
+
+def llmint8_read_outliers(workspace, K: int, stream=None):
+    """Synchronize and return the sorted outlier columns (int32 numpy array) left in `workspace`."""
+    import numpy as np
+    lib = _lib.load()
+    count = ctypes.c_int(0)
+    _check(lib.llmint8_read_outliers(_ptr(workspace), int(K), ctypes.byref(count), None, 0,
+                                     _stream(stream, workspace)), "llmint8_read_outliers")
+    out = np.zeros(max(count.value, 1), np.int32)
+    _check(lib.llmint8_read_outliers(_ptr(workspace), int(K), ctypes.byref(count),
+                                     out.ctypes.data_as(ctypes.c_void_p), out.size, _stream(stream, workspace)),
+           "llmint8_read_outliers")
+    return out[:count.value]
 
 
 def llmint8_pack_w16_rows(W16, rows, stream=None):

@@ -16,6 +16,7 @@
 #include "xpass.cuh"
 #include "wquant.cuh"
 #include "gemv.cuh"
+#include "gemv_stream.cuh"
 #include "gemm_tc.cuh"
 #include "chain.cuh"
 
@@ -93,6 +94,23 @@ llmint8_status encode_u8_2d(CUtensorMap* map, const void* base, int rows, int co
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? LLMINT8_OK : LLMINT8_ECUDA;
+}
+
+// int8 matrix [rows, K] (row pitch K bytes) as a 3D tensor: 64 bytes of K,
+// rows (stride K), 64-byte K steps (stride 64), K / 64 whole steps (a ragged
+// last step is not part of it).  A box of (64, box_rows, box_steps) lands in
+// shared memory as [box_steps][box_rows][64 bytes]; steps past the end are
+// filled with zeros.
+llmint8_status encode_u8_steps(CUtensorMap* map, const void* base, int rows, int K, int box_rows, int box_steps) {
+    const int steps = K / 64 > 0 ? K / 64 : 1;  // never loaded when K < 64
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)steps};
+    cuuint64_t strides[2] = {(cuuint64_t)K, 64};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_steps};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? LLMINT8_OK : LLMINT8_ECUDA;
@@ -259,11 +277,18 @@ bool rowq_gathers_w16(bool decode, int K, float threshold, bool write_i32, const
     return !decode && K <= 4096 && use_outliers && !write_i32 && W16 != nullptr;
 }
 
+// Caller-owned destinations of A2 (llmint8_quantize_x): int8 codes [M, K] and
+// row scales [M] in place of the workspace fields; no gathered outlier values.
+struct XpassOut {
+    int8_t* codes = nullptr;
+    float* row_scale = nullptr;
+};
+
 // A1 + A2 into the workspace; with gather_w16 also the A4 operand W16oT.
 template <typename T>
 llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* workspace, const Layout& L,
                             DeviceInfo* dev, cudaStream_t s, const void* W16 = nullptr, int N = 0,
-                            bool gather_w16 = false) {
+                            bool gather_w16 = false, const XpassOut& dst = XpassOut()) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
     const WsView w(workspace, L);
     const __half* Xh = static_cast<const __half*>(X);
@@ -300,10 +325,11 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
     ra.bitmap = w.bitmap;
     ra.hdr = w.hdr;
     ra.outlier_idx = w.idx;
-    ra.row_scale = w.row_scale;
-    ra.codes = w.codes;
-    ra.codes_fp16 = L.decode ? 0 : 1;  // int8 for the decode GEMV, fp16 values for the tensor-core GEMM
-    ra.xo = use_outliers ? w.xo : nullptr;
+    ra.row_scale = dst.codes ? dst.row_scale : w.row_scale;
+    ra.codes = dst.codes ? static_cast<void*>(dst.codes) : static_cast<void*>(w.codes);
+    // int8 for the decode GEMV (and caller buffers), fp16 values for the tensor-core GEMM
+    ra.codes_fp16 = (L.decode || dst.codes) ? 0 : 1;
+    ra.xo = (use_outliers && !dst.codes) ? w.xo : nullptr;
     ra.xo_pitch = L.kp;
     ra.no_outliers = use_outliers ? 0 : 1;
     ra.clear_status = (use_outliers && !cluster) ? 0 : 1;
@@ -326,6 +352,7 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
         return row_quant_vpt(K) == 1 ? launch_cluster(k_row_quant<1, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra)
                                      : launch_cluster(k_row_quant<2, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, cm, ra);
     }
+    if (dst.codes) gather_w16 = false;
     ra.W16 = gather_w16 ? static_cast<const __half*>(W16) : nullptr;
     ra.N = N;
     ra.w16o = gather_w16 ? w.w16o : nullptr;
@@ -370,50 +397,58 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         ga.M = M;
         ga.K = K;
         ga.N = N;
-        const int ksteps = (K + 63) / 64;
-        ga.k_per_warp = ((ksteps + kGemvWarps - 1) / kGemvWarps) * 64;
         ga.use_outliers = use_outliers ? 1 : 0;
         ga.w8 = src.w8 ? 1 : 0;
         ga.W16c = src.W16c;
         ga.row_map = src.row_map;
         ga.w16_rows = src.rows;
+        ga.hdr_err = w.hdr;
+        ga.spin_limit = kDefaultSpinLimit;
         {
             std::lock_guard<std::mutex> lock(g_mu);
             if (!dev->gemv_attr_set[Fmt<T>::kBF16]) {
-                const int m8 = (int)gemv_dyn_smem(8), m16 = (int)gemv_dyn_smem(16);
-                if (cudaFuncSetAttribute(k_gemv_decode<1, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
-                        cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<1, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
-                        cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<2, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
-                        cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode<2, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
-                        cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         m8) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         m8) != cudaSuccess)
+                const auto A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+                const int m = (int)(kGsSmemBudget + 128);
+                if (cudaFuncSetAttribute(k_gemv_stream<kGsDp4a, false, T>, A, m) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_stream<kGsDp4a, true, T>, A, m) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_stream<kGsMma1, false, T>, A, m) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_stream<kGsMma1, true, T>, A, m) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_stream<kGsMma2, false, T>, A, m) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_stream<kGsMma2, true, T>, A, m) != cudaSuccess)
                     return LLMINT8_ECUDA;
                 dev->gemv_attr_set[Fmt<T>::kBF16] = true;
             }
         }
-        const dim3 block(kGemvWarps * 32);
-        const int ntiles = N / kGemvCols, slots = 2 * dev->sms;  // two CTAs per SM
-        if (M <= 8) {
-            if (ntiles > slots) {  // one-tile CTAs would need several waves: persistent grid
-                const dim3 grid(slots);
-                return write_i32 ? launch(k_gemv_decode_tiles<1, true, T>, grid, block, gemv_dyn_smem(M), s, true, ga)
-                                 : launch(k_gemv_decode_tiles<1, false, T>, grid, block, gemv_dyn_smem(M), s, true, ga);
-            }
-            const dim3 grid(ntiles);
-            return write_i32 ? launch(k_gemv_decode<1, true, T>, grid, block, gemv_dyn_smem(M), s, true, ga)
-                             : launch(k_gemv_decode<1, false, T>, grid, block, gemv_dyn_smem(M), s, true, ga);
+        if ((st = get_encoder()) != LLMINT8_OK) return st;
+        // Wq [N, K] and the codes [M, K] as 3D tensors: 64 bytes of K, rows (stride K),
+        // 64-byte K steps (stride 64); boxes of one stage
+        const int mode = gs_mode(M), nst = gs_stage_k(mode) / 64;
+        CUtensorMap tm_w, tm_x;
+        if ((st = encode_u8_steps(&tm_w, Wq, N, K, kGsCols, nst)) != LLMINT8_OK) return st;
+        if ((st = encode_u8_steps(&tm_x, w.codes, M, K, M, nst)) != LLMINT8_OK) return st;
+        // one persistent CTA per SM, each streaming a contiguous run of at most
+        // kGsTilesMax tiles; wider N takes several launches over column blocks
+        const int ntiles = N / kGsCols;
+        const int per_launch = dev->sms * kGsTilesMax;
+        const dim3 block(kGsThreads);
+        for (int t0 = 0; t0 < ntiles; t0 += per_launch) {
+            const int nt = ntiles - t0 < per_launch ? ntiles - t0 : per_launch;
+            ga.n_base = t0 * kGsCols;
+            ga.ncols = nt * kGsCols;
+            const dim3 grid(nt < dev->sms ? nt : dev->sms);
+            const GsPlan plan = gs_plan(M, K, ga.ncols, (int)grid.x);
+            const size_t smem = gs_smem_bytes(plan);
+            if (plan.R < 2 || smem > kGsSmemBudget + 128) return LLMINT8_EUNSUPPORTED;
+            auto go = [&](auto kern) { return launch(kern, grid, block, smem, s, true, tm_w, tm_x, ga, plan); };
+            if (mode == kGsDp4a)
+                st = write_i32 ? go(k_gemv_stream<kGsDp4a, true, T>) : go(k_gemv_stream<kGsDp4a, false, T>);
+            else if (mode == kGsMma1)
+                st = write_i32 ? go(k_gemv_stream<kGsMma1, true, T>) : go(k_gemv_stream<kGsMma1, false, T>);
+            else
+                st = write_i32 ? go(k_gemv_stream<kGsMma2, true, T>) : go(k_gemv_stream<kGsMma2, false, T>);
+            if (st != LLMINT8_OK) return st;
         }
-        // up to 16 rows: the persistent form measured slower (its per-tile
-        // epilogue costs more than the waves it removes), one-tile CTAs
-        const dim3 grid(ntiles);
-        return write_i32 ? launch(k_gemv_decode<2, true, T>, grid, block, gemv_dyn_smem(M), s, true, ga)
-                         : launch(k_gemv_decode<2, false, T>, grid, block, gemv_dyn_smem(M), s, true, ga);
+        return LLMINT8_OK;
     }
 
     // A4 operand: gathered, transposed outlier rows of W16 (unless the X pass wrote it)
@@ -504,7 +539,15 @@ int kernels_per_call(int M, int K, int N, float threshold, bool write_i32) {
     int n = (scan ? 1 : 0) + 1 + 1;  // scan, row quant, GEMV / GEMM
     // outlier rows of W16 for the GEMM, unless the row quantization gathers them
     if (M > LLMINT8_DECODE_MAX_M && use_outliers && !write_i32 && K > 4096) n += 1;
-    (void)N;
+    if (M <= LLMINT8_DECODE_MAX_M) {
+        // the GEMV takes one launch per kGsTilesMax tiles per SM (148 SMs unless a
+        // device says otherwise)
+        int sms = 148, dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaGetLastError();  // no device here is not an error of this query
+        const long per = (long)(sms > 0 ? sms : 148) * kGsTilesMax;
+        n += (int)((N / kGsCols + per - 1) / per) - 1;
+    }
     return n;
 }
 
@@ -685,6 +728,26 @@ llmint8_status llmint8_matmul(const void* X, int M, int K, int N, float threshol
                        stream);
 }
 
+llmint8_status llmint8_matmul_host(const void* X_host, void* X, int M, int K, int N, float threshold,
+                                   const int8_t* Wq, const float* colScaleW, const void* Wq16, const void* W16, void* Y,
+                                   void* Y_host, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!X_host || !Y_host || !Y) return LLMINT8_EINVAL;
+    // every argument of the device call is checked before the first copy is enqueued
+    Layout L;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = check_common(X, M, K, N, threshold, workspace, workspace_bytes, &L, &dev);
+    if (st != LLMINT8_OK) return st;
+    if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, Y, false)) != LLMINT8_OK) return st;
+    if ((st = current_device(&dev)) != LLMINT8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(X, X_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess) return LLMINT8_ECUDA;
+    if ((st = llmint8_matmul(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, workspace, workspace_bytes, stream)) !=
+        LLMINT8_OK)
+        return st;
+    return cudaMemcpyAsync(Y_host, Y, (size_t)M * N * 2, cudaMemcpyDeviceToHost, s) == cudaSuccess ? LLMINT8_OK
+                                                                                                  : LLMINT8_ECUDA;
+}
+
 llmint8_status llmint8_matmul_w8(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
                                  const float* colScaleW, const void* Wq16, const void* W16c, const int32_t* row_map,
                                  int w16_rows, void* Y, void* workspace, size_t workspace_bytes, void* stream) {
@@ -741,6 +804,44 @@ llmint8_status llmint8_xpass(const void* X, int M, int K, int N, float threshold
     return xpass_launch<__half>(X, M, K, threshold, workspace, L, dev, static_cast<cudaStream_t>(stream));
 }
 
+llmint8_status llmint8_quantize_x(const void* X, int M, int K, float threshold, int8_t* Xq, float* rowScaleX,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    Layout L;
+    DeviceInfo* dev = nullptr;
+    // the workspace holds the outlier set; its codes field is not used (N = 16
+    // keeps the layout at its smallest)
+    llmint8_status st = check_common(X, M, K, 16, threshold, workspace, workspace_bytes, &L, &dev);
+    if (st != LLMINT8_OK) return st;
+    if (!Xq || !rowScaleX) return LLMINT8_EINVAL;
+    if (!aligned16(Xq) || !aligned16(rowScaleX)) return LLMINT8_EALIGN;
+    if ((st = current_device(&dev)) != LLMINT8_OK) return st;
+    XpassOut dst;
+    dst.codes = Xq;
+    dst.row_scale = rowScaleX;
+    return xpass_launch<__half>(X, M, K, threshold, workspace, L, dev, static_cast<cudaStream_t>(stream), nullptr, 0,
+                                false, dst);
+}
+
+llmint8_status llmint8_read_outliers(const void* workspace, int K, int* count, int32_t* idx_host, int capacity,
+                                     void* stream) {
+    if (!workspace || !count || K < 1 || K > kMaxK || capacity < 0 || (capacity > 0 && !idx_host))
+        return LLMINT8_EINVAL;
+    // the header and the outlier list sit at offsets that depend on K only
+    const Layout L = make_layout(1, K, 16);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LLMINT8_ECUDA;
+    const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+    int32_t n = 0;
+    if (cudaMemcpy(&n, ws + L.hdr + offsetof(WsHeader, outlier_count), 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LLMINT8_ECUDA;
+    if (n < 0 || n > K) return LLMINT8_EINVAL;  // not a workspace an X pass of this K filled
+    *count = n;
+    const int m = n < capacity ? n : capacity;
+    if (m > 0 && cudaMemcpy(idx_host, ws + L.idx, (size_t)m * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LLMINT8_ECUDA;
+    return LLMINT8_OK;
+}
+
 llmint8_status llmint8_gemm(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
                             const float* colScaleW, const void* Wq16, const void* W16, void* Y, void* workspace,
                             size_t workspace_bytes, void* stream) {
@@ -793,10 +894,11 @@ llmint8_status llmint8_chain_state_layout(int M, int N, size_t* offsets) {
     return LLMINT8_OK;
 }
 
-llmint8_status llmint8_matmul_chain(const void* X, int M, int K, int N, float threshold, const void* state_in,
-                                    const int8_t* Wq, const float* colScaleW, const void* W16, void* Y,
-                                    float next_threshold, void* state_out, void* workspace, size_t workspace_bytes,
-                                    void* stream) {
+// llmint8_matmul_chain and its int32 form (c_out set)
+static llmint8_status chain_impl(const void* X, int M, int K, int N, float threshold, const void* state_in,
+                          size_t state_in_bytes, const int8_t* Wq, const float* colScaleW, const void* W16, void* Y,
+                          float next_threshold, void* state_out, size_t state_out_bytes, int32_t* c_out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
     Layout L;
     DeviceInfo* dev = nullptr;
     // with a state in, its flags stand for the threshold (the argument is not used)
@@ -809,9 +911,12 @@ llmint8_status llmint8_matmul_chain(const void* X, int M, int K, int N, float th
     const bool use_outliers = !(std::isinf(t) && t > 0);
     if (use_outliers && !W16) return LLMINT8_EINVAL;
     if (!aligned16(Wq) || !aligned16(colScaleW) || !aligned16(Y) || (W16 && !aligned16(W16)) ||
-        (state_in && !aligned16(state_in)) || (state_out && !aligned16(state_out)))
+        (state_in && !aligned16(state_in)) || (state_out && !aligned16(state_out)) || (c_out && !aligned16(c_out)))
         return LLMINT8_EALIGN;
     if (!chain_shape_ok(M, K)) return LLMINT8_EUNSUPPORTED;
+    // the state buffers must hold the states this call reads and writes
+    if (state_in && state_in_bytes < chain_state_bytes(M, K)) return LLMINT8_EINVAL;
+    if (state_out && state_out_bytes < chain_state_bytes(M, N)) return LLMINT8_EINVAL;
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!state_in && (st = xpass_launch<__half>(X, M, K, threshold, workspace, L, dev, s, W16, N, false)) != LLMINT8_OK)
@@ -831,12 +936,13 @@ llmint8_status llmint8_matmul_chain(const void* X, int M, int K, int N, float th
     ga.M = M;
     ga.K = K;
     ga.N = N;
-    ga.k_per_warp = 0;
     ga.use_outliers = use_outliers ? 1 : 0;
     ga.w8 = 0;
     ga.W16c = nullptr;
     ga.row_map = nullptr;
     ga.w16_rows = 0;
+    ga.hdr_err = w.hdr;
+    ga.spin_limit = kDefaultSpinLimit;
     ChainArgs ch;
     ch.X = static_cast<const __half*>(X);
     ch.in = static_cast<const uint8_t*>(state_in);
@@ -844,7 +950,30 @@ llmint8_status llmint8_matmul_chain(const void* X, int M, int K, int N, float th
     ch.next_t = next_threshold;
     ch.err = w.hdr;
     ch.spin_limit = kDefaultSpinLimit;
+    ch.c_out = c_out;
+    ch.ws_codes = reinterpret_cast<int8_t*>(w.codes);
+    ch.ws_row_scale = w.row_scale;
+    ch.ws_idx = w.idx;
+    ch.ws_count = &w.hdr->outlier_count;
     return chain_launch(ga, ch, dev, s);
+}
+
+llmint8_status llmint8_matmul_chain(const void* X, int M, int K, int N, float threshold, const void* state_in,
+                                    size_t state_in_bytes, const int8_t* Wq, const float* colScaleW, const void* W16,
+                                    void* Y, float next_threshold, void* state_out, size_t state_out_bytes,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+    return chain_impl(X, M, K, N, threshold, state_in, state_in_bytes, Wq, colScaleW, W16, Y, next_threshold,
+                      state_out, state_out_bytes, nullptr, workspace, workspace_bytes, stream);
+}
+
+llmint8_status llmint8_matmul_chain_i32(const void* X, int M, int K, int N, float threshold, const void* state_in,
+                                        size_t state_in_bytes, const int8_t* Wq, const float* colScaleW,
+                                        const void* W16, void* Y, float next_threshold, void* state_out,
+                                        size_t state_out_bytes, int32_t* C, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+    if (!C) return LLMINT8_EINVAL;
+    return chain_impl(X, M, K, N, threshold, state_in, state_in_bytes, Wq, colScaleW, W16, Y, next_threshold,
+                      state_out, state_out_bytes, C, workspace, workspace_bytes, stream);
 }
 
 llmint8_status llmint8_selftest_timeout(void* workspace, int spin_limit, void* stream) {

@@ -3,8 +3,8 @@
 // In a decode step every matmul starts with the X pass of its input (A1, A2),
 // short kernels whose latency sits between the previous layer's GEMV and this
 // one; per-forward conversion of the activations is the cost the LLM.int8()
-// overview (section 3, small-batch performance) holds responsible for the
-// method's slowdown at small batch.  When the output Y of a GEMV is the next
+// paper walkthrough (section 5.4, small-batch performance) holds responsible
+// for the method's slowdown at small batch.  When the output Y of a GEMV is the next
 // layer's X, the GEMV's epilogue here computes what the next X pass would have
 // found from Y:
 //   * the outlier flags of Y's columns (A1: some row has |Y[i, j]| > t'), and
@@ -82,7 +82,16 @@ struct ChainArgs {
     float next_t;          // threshold the flags of Y are taken for
     WsHeader* err;         // error word
     uint32_t spin_limit;   // poll budget of the bounded waits
+    int32_t* c_out;        // [M, N] exact int32 accumulator of A3, or nullptr
+    // workspace fields of the X pass: with a chain state in, CTA 0 leaves there
+    // what it derived (the same fields an X pass fills)
+    int8_t* ws_codes;      // [M, K]
+    float* ws_row_scale;   // [M]
+    int32_t* ws_idx;       // [K] outlier columns, ascending
+    int32_t* ws_count;     // outlier count
 };
+
+constexpr uint32_t kStatusInvalid = 1;  // == LLMINT8_EINVAL: a chain state that does not fit the call
 
 struct ChainBars {
     uint64_t full[kChainStages];
@@ -190,7 +199,7 @@ __global__ void __launch_bounds__(kChainThreads, 2)
             if (t == S) issue_x();
             // stages of the first round are free; later ones wait for the 8 consumer warps
             if (t >= S && !mbar_wait_bounded(&sb->empty[q], ph ^ 1u, ch.spin_limit, abort_flag)) {
-                fail(21);
+                if (!*abort_flag) fail(21);  // a wait that ran out, not consumers that left
                 ok = false;
                 break;
             }
@@ -206,12 +215,13 @@ __global__ void __launch_bounds__(kChainThreads, 2)
             if (++st == sps) st = 0, ++j;
         }
         if (!x_issued) issue_x();
-        if (!ok) {
-            // let copies already in flight land before the CTA can end
-            for (int s = 0; s < S; ++s)
-                if ((issued >> s) & 1u) mbar_wait_bounded(&sb->full[s], (issued_par >> s) & 1u, 1u << 20, nullptr);
-            if (!IN_RAW) mbar_wait_bounded(&sb->xbar, 0, 1u << 20, nullptr);
-        }
+        // no copy may still target shared memory when the CTA ends, whether the
+        // consumers finished or left early: wait for the last fill of every stage
+        // (already complete on the normal path) and for the codes
+        for (int s = 0; s < S; ++s)
+            if ((issued >> s) & 1u) mbar_wait_bounded(&sb->full[s], (issued_par >> s) & 1u, 1u << 20, nullptr);
+        if (!IN_RAW) mbar_wait_bounded(&sb->xbar, 0, 1u << 20, nullptr);
+        (void)ok;
         return;
     }
 
@@ -235,7 +245,24 @@ __global__ void __launch_bounds__(kChainThreads, 2)
         // scales, and the codes of X into shared memory ----
         const uint8_t* flags = ch.in + chain_flags_off();
         const float* parts = reinterpret_cast<const float*>(ch.in + chain_parts_off(K));
-        const int nparts = ldg_cg_s32(&reinterpret_cast<const ChainHeader*>(ch.in)->nparts);
+        // the header must describe an activation of this call's shape: M rows,
+        // K columns, and at most one partial maximum per 16-column strip (the
+        // host checked that the buffer holds that many); nothing else of the
+        // state is read otherwise
+        if (blockIdx.x == 0 && tid == 0) ch.err->status = 0u;  // no X pass ran to clear the error word
+        const ChainHeader* hin = reinterpret_cast<const ChainHeader*>(ch.in);
+        const int hM = ldg_cg_s32(&hin->M), hN = ldg_cg_s32(&hin->N);
+        const int nparts = ldg_cg_s32(&hin->nparts);
+        if (hM != MR || hN != K || nparts < 1 || nparts > K / kChainCols) {
+            // every CTA leaves; CTA 0 alone records it, after clearing the word
+            // above, so no earlier write can hide it (the producers, stopped by
+            // the flag, record nothing)
+            if (tid == 0) {
+                if (blockIdx.x == 0) record_error(ch.err, kStatusInvalid, 26);
+                *abort_flag = 1u;
+            }
+            return;
+        }
         // bit-map words: each thread takes a contiguous run of words
         const int wpt = (nwords + kChainWarps * 32 - 1) / (kChainWarps * 32);
         const int w0 = min(nwords, tid * wpt), w1 = min(nwords, w0 + wpt);
@@ -316,6 +343,21 @@ __global__ void __launch_bounds__(kChainThreads, 2)
             }
         }
         chain_consumer_sync();  // codes, bit map and prefix counts visible to all consumer warps
+        if (blockIdx.x == 0) {
+            // what this call derived, into the workspace fields an X pass fills
+            for (int c = 16 * tid; c < MR * K; c += 16 * kChainWarps * 32)
+                *reinterpret_cast<uint4*>(ch.ws_codes + c) = *reinterpret_cast<const uint4*>(xs + c);
+            if (tid < MR) ch.ws_row_scale[tid] = s_sx[tid];
+            for (int w = w0; w < w1; ++w) {
+                uint32_t b = s_bits[w];
+                int pos = s_prefix[w];
+                while (b) {
+                    ch.ws_idx[pos++] = 32 * w + __ffs(b) - 1;
+                    b &= b - 1;
+                }
+            }
+            if (tid == 0) *ch.ws_count = s_total;
+        }
     } else {
         cnt = outl ? ldg_cg_s32(&a.hdr->outlier_count) : 0;
     }
@@ -478,6 +520,7 @@ __global__ void __launch_bounds__(kChainThreads, 2)
             const __half y0 = __float2half_rn(fmaf((float)c0, rs * cs0 * k2, f0));
             const __half y1 = __float2half_rn(fmaf((float)c1, rs * cs1 * k2, f1));
             *reinterpret_cast<__half2*>(reinterpret_cast<__half*>(a.out) + (size_t)oi * N + nA) = __halves2half2(y0, y1);
+            if (ch.c_out != nullptr) *reinterpret_cast<int2*>(ch.c_out + (size_t)oi * N + nA) = make_int2(c0, c1);
             y0f = fabsf(__half2float(y0));
             y1f = fabsf(__half2float(y1));
         }

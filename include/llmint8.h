@@ -107,6 +107,29 @@ llmint8_status llmint8_matmul(const void *X, int M, int K, int N, float threshol
                               void *stream);
 
 /*
+ * llmint8_matmul between host buffers: enqueues on `stream` the copy of X_host
+ * into the device buffer X, the same kernels as llmint8_matmul, and the copy of
+ * Y into Y_host, then returns (asynchronous: synchronize the stream before
+ * reading Y_host).  For callers whose activations and results live in host
+ * memory; one call instead of three.
+ *
+ *   X_host  in   host fp16 [M, K] (page-locked memory keeps the copies
+ *                asynchronous; pageable memory works but the copies then
+ *                block the calling thread)
+ *   X       out  device fp16 [M, K] staging buffer (receives X_host)
+ *   Y       out  device fp16 [M, N]
+ *   Y_host  out  host fp16 [M, N]
+ *   other arguments as llmint8_matmul
+ *
+ * Errors as llmint8_matmul (all checked before the first copy is enqueued);
+ * EINVAL also for a NULL X_host, Y_host or Y; ECUDA if a copy cannot be enqueued.
+ */
+llmint8_status llmint8_matmul_host(const void *X_host, void *X, int M, int K, int N, float threshold,
+                                   const int8_t *Wq, const float *colScaleW, const void *Wq16,
+                                   const void *W16, void *Y, void *Y_host, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * bfloat16 forms: the same steps on bf16 W, X and Y (all other arguments as the
  * fp16 entry points).  The codes, scales, outlier test and the int32 product are
  * computed from the fp32 values of the bf16 inputs exactly as from fp16 ones;
@@ -206,14 +229,45 @@ llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold,
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * A1 + A2 into caller buffers (the pages' quantization of the activations,
+ * paper walkthrough sections 2.1 and 2.3; pitfalls guide, section 1):
+ *   Xq         out  int8 [M, K] row-major codes, outlier columns 0
+ *   rowScaleX  out  fp32 [M], absmax of each row over the non-outlier columns
+ *   workspace  scratch of at least llmint8_workspace_bytes(M, K, 16) bytes; it
+ *              receives the outlier column set (llmint8_read_outliers)
+ * Same rules as llmint8_matmul for X, M, K and threshold; EINVAL for a NULL Xq
+ * or rowScaleX, EALIGN for one that is not 16-byte aligned.  Asynchronous.
+ */
+llmint8_status llmint8_quantize_x(const void *X, int M, int K, float threshold, int8_t *Xq, float *rowScaleX,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronizes `stream`, then copies the outlier column set (A1, paper
+ * walkthrough section 2.3) that the last llmint8_quantize_x / llmint8_matmul*
+ * call on `workspace` found for rows of K columns:
+ *   count     out  number of outlier columns (host int)
+ *   idx_host  out  host int32 [capacity]: the first min(count, capacity)
+ *                  column indices, ascending (may be NULL when capacity = 0)
+ * EINVAL for NULL workspace or count, K outside [1, 65536], capacity < 0, or a
+ * stored count outside [0, K] (a workspace no X pass of this K has filled);
+ * ECUDA if synchronization or a copy fails.
+ */
+llmint8_status llmint8_read_outliers(const void *workspace, int K, int *count, int32_t *idx_host, int capacity,
+                                     void *stream);
+
+/*
  * Decode chain (1 <= M <= 4 rows, fp16): a matmul whose GEMV also prepares the
  * X pass of the next layer, when its output Y is that layer's input.  The
  * pages place the small-batch cost of the method in the per-forward handling
- * of the activations (LLM.int8() overview, section 3); here the outlier
- * columns of Y (A1 for the next threshold, paper walkthrough section 2.1) and
- * the row absmax of Y over the other columns (A2, section 2.3) are computed in
- * the GEMV's epilogue and left in a "chain state", so the next call runs one
- * kernel and no X pass.  Results are those of llmint8_matmul on the same X.
+ * of the activations (paper walkthrough, section 5.4); here the outlier
+ * columns of Y (A1 for the next threshold, paper walkthrough section 2.3) and
+ * the row absmax of Y over the other columns (A2: sections 2.1 and 2.3) are
+ * computed in the GEMV's epilogue and left in a "chain state", so the next call
+ * runs one kernel and no X pass.  The codes, row scales and outlier set are
+ * those llmint8_matmul derives from the same X (bit for bit; after a call given
+ * a state they are left in the workspace fields of llmint8_workspace_layout),
+ * and Y agrees with llmint8_matmul's within the stated tolerance (the outlier
+ * slice is summed in another order).
  *
  *   X               in   fp16 [M, K] device (the previous layer's Y)
  *   threshold       in   outlier threshold of X, used only without state_in
@@ -224,13 +278,20 @@ llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold,
  *   next_threshold  in   threshold the flags of Y are taken for (not NaN)
  *   state_out       out  chain state of Y (llmint8_chain_state_bytes(M, N)
  *                        bytes, 16-byte aligned), or NULL
+ *   state_in_bytes, state_out_bytes
+ *                   in   sizes of the two state buffers (ignored for a NULL
+ *                        state): at least llmint8_chain_state_bytes(M, K) and
+ *                        llmint8_chain_state_bytes(M, N), else LLMINT8_EINVAL
  *   workspace       scratch as llmint8_matmul (error word, X-pass results)
  *
  * Chain state layout (llmint8_chain_state_layout): a 256-byte header (int32 M,
  * N, nparts, float threshold), then uint8 flags [N] (1 = outlier column, 0 =
  * not; no other values), then float [nparts][M] partial row maxima (the row
  * scale is their maximum; non-negative).  A caller may fill one by hand with
- * nparts = 1; M and N in the header must match the call that reads it.
+ * nparts = 1; M and N in the header must match the call that reads it (M and
+ * K of that call) and 1 <= nparts <= N / 16.  The kernel checks this header
+ * before it reads anything else of the state: a mismatch leaves Y unwritten and
+ * records LLMINT8_EINVAL in the workspace error word (llmint8_device_status).
  *
  * Errors as llmint8_matmul; EUNSUPPORTED for M > 4, K < 512, or M * K too
  * large for shared memory; EINVAL if state_in == state_out, W16 is NULL while
@@ -242,9 +303,21 @@ llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold,
 size_t llmint8_chain_state_bytes(int M, int N);
 llmint8_status llmint8_chain_state_layout(int M, int N, size_t *offsets /* [3]: flags, parts, total */);
 llmint8_status llmint8_matmul_chain(const void *X, int M, int K, int N, float threshold, const void *state_in,
-                                    const int8_t *Wq, const float *colScaleW, const void *W16, void *Y,
-                                    float next_threshold, void *state_out, void *workspace,
-                                    size_t workspace_bytes, void *stream);
+                                    size_t state_in_bytes, const int8_t *Wq, const float *colScaleW,
+                                    const void *W16, void *Y, float next_threshold, void *state_out,
+                                    size_t state_out_bytes, void *workspace, size_t workspace_bytes,
+                                    void *stream);
+/*
+ * llmint8_matmul_chain that also writes the exact int32 accumulator of step A3,
+ * C int32 [M, N] = sum_k Xq[i,k] * Wq[n,k] (introspection: the codes the chain
+ * kernel derives from a state are then checkable bit for bit).  Same arguments
+ * and errors, plus C (16-byte aligned, not NULL).
+ */
+llmint8_status llmint8_matmul_chain_i32(const void *X, int M, int K, int N, float threshold, const void *state_in,
+                                        size_t state_in_bytes, const int8_t *Wq, const float *colScaleW,
+                                        const void *W16, void *Y, float next_threshold, void *state_out,
+                                        size_t state_out_bytes, int32_t *C, void *workspace,
+                                        size_t workspace_bytes, void *stream);
 
 /*
  * Allocation-free variant of llmint8_matmul.  The pages describe no such call;
@@ -296,11 +369,13 @@ llmint8_status llmint8_matmul_i32(const void *X, int M, int K, int N, float thre
  * M <= 16 with K <= 4096, where the row-quantization CTAs form one cluster and
  * find the outlier columns themselves), the row quantization, for M > 16 with a
  * finite threshold, write_i32 = 0 and K > 4096 the gather of the outlier rows
- * of W16 (for K <= 4096 the row quantization writes them), and the GEMV or GEMM.
- * The bf16 entry points launch the same kernels; llmint8_matmul_w8 launches the
- * gather for every M > 16 with a finite threshold (one more kernel when
- * K <= 4096).  -1 for arguments the call would reject as EINVAL.
- * Host-only; touches no device.
+ * of W16 (for K <= 4096 the row quantization writes them), and the GEMV or GEMM
+ * (the GEMV as one launch per 16 x (SM count) 16-column tiles: one for every N
+ * up to 37888 on a 148-SM part).  The bf16 entry points launch the same
+ * kernels; llmint8_matmul_w8 launches the gather for every M > 16 with a finite
+ * threshold (one more kernel when K <= 4096).  -1 for arguments the call would
+ * reject as EINVAL.  Host-only: it reads the current device's SM count when
+ * there is one (148 otherwise).
  */
 int llmint8_kernels_per_call(int M, int K, int N, float threshold, int write_i32);
 

@@ -115,10 +115,12 @@ def test_noalloc_argument_errors(lib):
                                       P(FAKE), None) == _lib.EINVAL
 
 
-def _chain(lib, M=1, K=4096, N=4096, t=6.0, sin=0, w16=FAKE, nt=6.0, sout=FAKE + 4096, Y=FAKE, wsb=1 << 40):
+def _chain(lib, M=1, K=4096, N=4096, t=6.0, sin=0, w16=FAKE, nt=6.0, sout=FAKE + 4096, Y=FAKE, wsb=1 << 40,
+           sinb=1 << 30, soutb=1 << 30):
     P = ctypes.c_void_p
-    return lib.llmint8_matmul_chain(P(FAKE), M, K, N, t, P(sin) if sin else None, P(FAKE), P(FAKE),
-                                    P(w16) if w16 else None, P(Y), nt, P(sout) if sout else None, P(FAKE), wsb, None)
+    return lib.llmint8_matmul_chain(P(FAKE), M, K, N, t, P(sin) if sin else None, sinb, P(FAKE), P(FAKE),
+                                    P(w16) if w16 else None, P(Y), nt, P(sout) if sout else None, soutb, P(FAKE),
+                                    wsb, None)
 
 
 def test_chain_state_layout(lib):
@@ -143,6 +145,52 @@ def test_chain_argument_errors(lib):
     assert _chain(lib, sin=FAKE + 8) == _lib.EALIGN
     assert _chain(lib, t=math.nan) == _lib.EINVAL
     assert _chain(lib, wsb=16) == _lib.EWORKSPACE
+    # state buffers smaller than the states the call reads or writes
+    need_in = lib.llmint8_chain_state_bytes(1, 4096)
+    assert _chain(lib, sin=FAKE + (1 << 20), sinb=need_in - 16) == _lib.EINVAL
+    assert _chain(lib, N=11008, soutb=lib.llmint8_chain_state_bytes(1, 11008) - 1) == _lib.EINVAL
+    P = ctypes.c_void_p
+    assert lib.llmint8_matmul_chain_i32(P(FAKE), 1, 4096, 4096, 6.0, None, 0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                        6.0, None, 0, None, P(FAKE), 1 << 40, None) == _lib.EINVAL  # no C
+    assert lib.llmint8_matmul_chain_i32(P(FAKE), 1, 4096, 4096, 6.0, None, 0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                        6.0, None, 0, P(FAKE + 4), P(FAKE), 1 << 40, None) == _lib.EALIGN
+
+
+def test_matmul_host_argument_errors(lib):
+    P = ctypes.c_void_p
+    ws = lib.llmint8_workspace_bytes(4, 64, 64)
+    call = lambda xh=FAKE, yh=FAKE, Y=FAKE, M=4, wsb=ws: lib.llmint8_matmul_host(
+        P(xh) if xh else None, P(FAKE), M, 64, 64, 6.0, P(FAKE), P(FAKE), None, P(FAKE), P(Y) if Y else None,
+        P(yh) if yh else None, P(FAKE), wsb, None)
+    assert call(xh=0) == _lib.EINVAL
+    assert call(yh=0) == _lib.EINVAL
+    assert call(Y=0) == _lib.EINVAL
+    assert call(M=0) == _lib.EINVAL
+    assert call(wsb=16) == _lib.EWORKSPACE
+
+
+def test_quantize_x_and_read_outliers_argument_errors(lib):
+    P = ctypes.c_void_p
+    ws = lib.llmint8_workspace_bytes(4, 64, 16)
+    q = lambda X=FAKE, M=4, K=64, t=6.0, Xq=FAKE, rs=FAKE, wsb=ws: lib.llmint8_quantize_x(
+        P(X) if X else None, M, K, t, P(Xq) if Xq else None, P(rs) if rs else None, P(FAKE), wsb, None)
+    assert q(X=0) == _lib.EINVAL
+    assert q(M=0) == _lib.EINVAL
+    assert q(K=70000) == _lib.EINVAL
+    assert q(t=math.nan) == _lib.EINVAL
+    assert q(Xq=0) == _lib.EINVAL
+    assert q(rs=0) == _lib.EINVAL
+    assert q(K=72) == _lib.EALIGN
+    assert q(Xq=FAKE + 8) == _lib.EALIGN
+    assert q(wsb=ws - 16) == _lib.EWORKSPACE
+    n = ctypes.c_int(0)
+    r = lib.llmint8_read_outliers
+    assert r(None, 64, ctypes.byref(n), None, 0, None) == _lib.EINVAL
+    assert r(P(FAKE), 64, None, None, 0, None) == _lib.EINVAL
+    assert r(P(FAKE), 0, ctypes.byref(n), None, 0, None) == _lib.EINVAL
+    assert r(P(FAKE), 70000, ctypes.byref(n), None, 0, None) == _lib.EINVAL
+    assert r(P(FAKE), 64, ctypes.byref(n), None, -1, None) == _lib.EINVAL
+    assert r(P(FAKE), 64, ctypes.byref(n), None, 4, None) == _lib.EINVAL  # capacity without a buffer
 
 
 def test_selftest_argument_errors(lib):
