@@ -16,7 +16,6 @@
 #include "xpass.cuh"
 #include "wquant.cuh"
 #include "gemv.cuh"
-#include "gemv_stream.cuh"
 #include "gemm_tc.cuh"
 #include "chain.cuh"
 
@@ -94,23 +93,6 @@ llmint8_status encode_u8_2d(CUtensorMap* map, const void* base, int rows, int co
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? LLMINT8_OK : LLMINT8_ECUDA;
-}
-
-// int8 matrix [rows, K] (row pitch K bytes) as a 3D tensor: 64 bytes of K,
-// rows (stride K), 64-byte K steps (stride 64), K / 64 whole steps (a ragged
-// last step is not part of it).  A box of (64, box_rows, box_steps) lands in
-// shared memory as [box_steps][box_rows][64 bytes]; steps past the end are
-// filled with zeros.
-llmint8_status encode_u8_steps(CUtensorMap* map, const void* base, int rows, int K, int box_rows, int box_steps) {
-    const int steps = K / 64 > 0 ? K / 64 : 1;  // never loaded when K < 64
-    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)steps};
-    cuuint64_t strides[2] = {(cuuint64_t)K, 64};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_steps};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? LLMINT8_OK : LLMINT8_ECUDA;
@@ -397,58 +379,50 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         ga.M = M;
         ga.K = K;
         ga.N = N;
+        const int ksteps = (K + 63) / 64;
+        ga.k_per_warp = ((ksteps + kGemvWarps - 1) / kGemvWarps) * 64;
         ga.use_outliers = use_outliers ? 1 : 0;
         ga.w8 = src.w8 ? 1 : 0;
         ga.W16c = src.W16c;
         ga.row_map = src.row_map;
         ga.w16_rows = src.rows;
-        ga.hdr_err = w.hdr;
-        ga.spin_limit = kDefaultSpinLimit;
         {
             std::lock_guard<std::mutex> lock(g_mu);
             if (!dev->gemv_attr_set[Fmt<T>::kBF16]) {
-                const auto A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-                const int m = (int)(kGsSmemBudget + 128);
-                if (cudaFuncSetAttribute(k_gemv_stream<kGsDp4a, false, T>, A, m) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_stream<kGsDp4a, true, T>, A, m) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_stream<kGsMma1, false, T>, A, m) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_stream<kGsMma1, true, T>, A, m) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_stream<kGsMma2, false, T>, A, m) != cudaSuccess ||
-                    cudaFuncSetAttribute(k_gemv_stream<kGsMma2, true, T>, A, m) != cudaSuccess)
+                const int m8 = (int)gemv_dyn_smem(8), m16 = (int)gemv_dyn_smem(16);
+                if (cudaFuncSetAttribute(k_gemv_decode<1, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<1, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m8) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<2, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode<2, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, m16) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         m8) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemv_decode_tiles<1, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         m8) != cudaSuccess)
                     return LLMINT8_ECUDA;
                 dev->gemv_attr_set[Fmt<T>::kBF16] = true;
             }
         }
-        if ((st = get_encoder()) != LLMINT8_OK) return st;
-        // Wq [N, K] and the codes [M, K] as 3D tensors: 64 bytes of K, rows (stride K),
-        // 64-byte K steps (stride 64); boxes of one stage
-        const int mode = gs_mode(M), nst = gs_stage_k(mode) / 64;
-        CUtensorMap tm_w, tm_x;
-        if ((st = encode_u8_steps(&tm_w, Wq, N, K, kGsCols, nst)) != LLMINT8_OK) return st;
-        if ((st = encode_u8_steps(&tm_x, w.codes, M, K, M, nst)) != LLMINT8_OK) return st;
-        // one persistent CTA per SM, each streaming a contiguous run of at most
-        // kGsTilesMax tiles; wider N takes several launches over column blocks
-        const int ntiles = N / kGsCols;
-        const int per_launch = dev->sms * kGsTilesMax;
-        const dim3 block(kGsThreads);
-        for (int t0 = 0; t0 < ntiles; t0 += per_launch) {
-            const int nt = ntiles - t0 < per_launch ? ntiles - t0 : per_launch;
-            ga.n_base = t0 * kGsCols;
-            ga.ncols = nt * kGsCols;
-            const dim3 grid(nt < dev->sms ? nt : dev->sms);
-            const GsPlan plan = gs_plan(M, K, ga.ncols, (int)grid.x);
-            const size_t smem = gs_smem_bytes(plan);
-            if (plan.R < 2 || smem > kGsSmemBudget + 128) return LLMINT8_EUNSUPPORTED;
-            auto go = [&](auto kern) { return launch(kern, grid, block, smem, s, true, tm_w, tm_x, ga, plan); };
-            if (mode == kGsDp4a)
-                st = write_i32 ? go(k_gemv_stream<kGsDp4a, true, T>) : go(k_gemv_stream<kGsDp4a, false, T>);
-            else if (mode == kGsMma1)
-                st = write_i32 ? go(k_gemv_stream<kGsMma1, true, T>) : go(k_gemv_stream<kGsMma1, false, T>);
-            else
-                st = write_i32 ? go(k_gemv_stream<kGsMma2, true, T>) : go(k_gemv_stream<kGsMma2, false, T>);
-            if (st != LLMINT8_OK) return st;
+        const dim3 block(kGemvWarps * 32);
+        const int ntiles = N / kGemvCols, slots = 2 * dev->sms;  // two CTAs per SM
+        if (M <= 8) {
+            if (ntiles > slots) {  // one-tile CTAs would need several waves: persistent grid
+                const dim3 grid(slots);
+                return write_i32 ? launch(k_gemv_decode_tiles<1, true, T>, grid, block, gemv_dyn_smem(M), s, true, ga)
+                                 : launch(k_gemv_decode_tiles<1, false, T>, grid, block, gemv_dyn_smem(M), s, true, ga);
+            }
+            const dim3 grid(ntiles);
+            return write_i32 ? launch(k_gemv_decode<1, true, T>, grid, block, gemv_dyn_smem(M), s, true, ga)
+                             : launch(k_gemv_decode<1, false, T>, grid, block, gemv_dyn_smem(M), s, true, ga);
         }
-        return LLMINT8_OK;
+        // up to 16 rows: the persistent form measured slower (its per-tile
+        // epilogue costs more than the waves it removes), one-tile CTAs
+        const dim3 grid(ntiles);
+        return write_i32 ? launch(k_gemv_decode<2, true, T>, grid, block, gemv_dyn_smem(M), s, true, ga)
+                         : launch(k_gemv_decode<2, false, T>, grid, block, gemv_dyn_smem(M), s, true, ga);
     }
 
     // A4 operand: gathered, transposed outlier rows of W16 (unless the X pass wrote it)
@@ -539,15 +513,7 @@ int kernels_per_call(int M, int K, int N, float threshold, bool write_i32) {
     int n = (scan ? 1 : 0) + 1 + 1;  // scan, row quant, GEMV / GEMM
     // outlier rows of W16 for the GEMM, unless the row quantization gathers them
     if (M > LLMINT8_DECODE_MAX_M && use_outliers && !write_i32 && K > 4096) n += 1;
-    if (M <= LLMINT8_DECODE_MAX_M) {
-        // the GEMV takes one launch per kGsTilesMax tiles per SM (148 SMs unless a
-        // device says otherwise)
-        int sms = 148, dev = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaGetLastError();  // no device here is not an error of this query
-        const long per = (long)(sms > 0 ? sms : 148) * kGsTilesMax;
-        n += (int)((N / kGsCols + per - 1) / per) - 1;
-    }
+    (void)N;
     return n;
 }
 
@@ -941,8 +907,7 @@ static llmint8_status chain_impl(const void* X, int M, int K, int N, float thres
     ga.W16c = nullptr;
     ga.row_map = nullptr;
     ga.w16_rows = 0;
-    ga.hdr_err = w.hdr;
-    ga.spin_limit = kDefaultSpinLimit;
+    ga.k_per_warp = 0;
     ChainArgs ch;
     ch.X = static_cast<const __half*>(X);
     ch.in = static_cast<const uint8_t*>(state_in);

@@ -369,13 +369,11 @@ llmint8_status llmint8_matmul_i32(const void *X, int M, int K, int N, float thre
  * M <= 16 with K <= 4096, where the row-quantization CTAs form one cluster and
  * find the outlier columns themselves), the row quantization, for M > 16 with a
  * finite threshold, write_i32 = 0 and K > 4096 the gather of the outlier rows
- * of W16 (for K <= 4096 the row quantization writes them), and the GEMV or GEMM
- * (the GEMV as one launch per 16 x (SM count) 16-column tiles: one for every N
- * up to 37888 on a 148-SM part).  The bf16 entry points launch the same
- * kernels; llmint8_matmul_w8 launches the gather for every M > 16 with a finite
- * threshold (one more kernel when K <= 4096).  -1 for arguments the call would
- * reject as EINVAL.  Host-only: it reads the current device's SM count when
- * there is one (148 otherwise).
+ * of W16 (for K <= 4096 the row quantization writes them), and the GEMV or GEMM.
+ * The bf16 entry points launch the same kernels; llmint8_matmul_w8 launches the
+ * gather for every M > 16 with a finite threshold (one more kernel when
+ * K <= 4096).  -1 for arguments the call would reject as EINVAL.
+ * Host-only; touches no device.
  */
 int llmint8_kernels_per_call(int M, int K, int N, float threshold, int write_i32);
 

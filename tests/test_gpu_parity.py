@@ -62,6 +62,8 @@ def test_decode_long_k(M, K, N):
     (1, 64, 600, 0.05),      # one K step: only warp 0 streams; three or four tiles per CTA
     (4, 11008, 40, 0.001),
     (16, 1040, 400, 0.05),   # more than 8 rows: one-tile CTAs in several waves
+    (1, 2048, 150, 0.2),     # ~410 outliers: the persistent GEMV stages six more chunks per tile
+    (8, 1040, 200, 0.45),    # ~470 outliers, the last chunk partial
 ])
 def test_decode_many_tiles(M, K, extra_tiles, frac):
     # More 16-column tiles than two CTAs per SM.  Up to 8 rows of X this is the

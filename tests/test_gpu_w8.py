@@ -57,12 +57,13 @@ def test_w8_against_oracle(M, K, N, keep, frac):
     _run(M, K, N, keep, frac, seed=M + K + N)
 
 
-@pytest.mark.parametrize("M,keep", [(2, "none"), (8, "some")])
-def test_w8_persistent_gemv(M, keep):
+@pytest.mark.parametrize("M,keep,frac", [(2, "none", 0.05), (8, "some", 0.05), (4, "some", 0.2)])
+def test_w8_persistent_gemv(M, keep, frac):
     # more 16-column tiles than two CTAs per SM: the persistent GEMV stages the
-    # outlier rows tile by tile
+    # outlier rows tile by tile (frac 0.2: ~218 outliers, several chunks per tile,
+    # kept and dequantized rows mixed)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    _run(M, 1088, 16 * (2 * sms + 60), keep, 0.05, seed=300 + M)
+    _run(M, 1088, 16 * (2 * sms + 60), keep, frac, seed=300 + M)
 
 
 @pytest.mark.parametrize("M", [3, 200])
