@@ -219,7 +219,7 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------------------- our arm
 
 KERNEL_SOURCES = {  # the sources each timed kernel is compiled from
-    "k_gemv_stream": ("gemv_stream.cuh", "gemv.cuh", "common.cuh"),
+    "k_gemv_decode": ("gemv.cuh", "common.cuh"),
 }
 
 
@@ -266,7 +266,7 @@ def run_ours(args, world, rank, local):
         W, _ = c.w()
         Xd = torch.from_numpy(X).to(dev)
         Wd = torch.from_numpy(W).to(dev)
-        Wq, sw, _ = api.llmint8_quantize_weight(Wd, fp16_codes=False)
+        Wq, sw = api.llmint8_quantize_weight(Wd)
         reps = [(Wq, sw, Wd)] + [(Wq.clone(), sw.clone(), Wd.clone()) for _ in range(R - 1)]
         ws = api.make_workspace(c.M, c.K, c.N, dev)
         Y = torch.empty((c.M, c.N), dtype=torch.float16, device=dev)
@@ -275,7 +275,7 @@ def run_ours(args, world, rank, local):
     # realised outlier counts (deterministic for these inputs) -> algorithmic bytes
     for d in cases:
         c = d["c"]
-        api.llmint8_matmul(d["Xd"], c.threshold, *d["reps"][0][:2], None, d["reps"][0][2], Y=d["Y"], workspace=d["ws"])
+        api.llmint8_matmul(d["Xd"], c.threshold, *d["reps"][0], Y=d["Y"], workspace=d["ws"])
     torch.cuda.synchronize()
     step_bytes = 0
     for d in cases:
@@ -291,7 +291,9 @@ def run_ours(args, world, rank, local):
     for d in cases:
         c = d["c"]
         d["kpc"] = api.llmint8_kernels_per_call(c.M, c.K, c.N, c.threshold)
-        d["kernel"] = "k_gemv_stream"  # the decode GEMV: one persistent CTA per SM
+        # the decode GEMV: one 16-column tile per CTA, or a persistent grid of two
+        # CTAs per SM when M <= 8 and the tiles would need several waves
+        d["kernel"] = "k_gemv_decode_tiles" if c.M <= 8 and c.N // 16 > 2 * sms else "k_gemv_decode"
     launches_per_step = sum(d["kpc"] for d in cases)
 
     # ---- one CUDA graph per step (the 9 llmint8_matmul calls), so the GPU is not
@@ -308,10 +310,10 @@ def run_ours(args, world, rank, local):
                 if instrumented:  # xpass, [event], GEMV, [event]
                     api.llmint8_xpass(d["Xd"], c.threshold, c.N, d["ws"])
                     evs[ci][0].record()
-                    api.llmint8_gemm(d["Xd"], c.threshold, Wq, sw, None, Wd, d["Y"], d["ws"])
+                    api.llmint8_gemm(d["Xd"], c.threshold, Wq, sw, Wd, d["Y"], d["ws"])
                     evs[ci][1].record()
                 else:
-                    api.llmint8_matmul(d["Xd"], c.threshold, Wq, sw, None, Wd, Y=d["Y"], workspace=d["ws"])
+                    api.llmint8_matmul(d["Xd"], c.threshold, Wq, sw, Wd, Y=d["Y"], workspace=d["ws"])
         return g, evs
 
     G = min(args.steps, args.max_graphs)
@@ -364,7 +366,7 @@ def run_ours(args, world, rank, local):
         with torch.cuda.graph(g):
             for r in range(B):
                 Wq, sw, Wd = d["reps"][r % R]
-                api.llmint8_gemm(d["Xd"], c.threshold, Wq, sw, None, Wd, d["Y"], d["ws"])
+                api.llmint8_gemm(d["Xd"], c.threshold, Wq, sw, Wd, d["Y"], d["ws"])
         for _ in range(2):
             g.replay()
         torch.cuda.synchronize()
@@ -387,7 +389,7 @@ def run_ours(args, world, rank, local):
                   "frac": d["bytes"] / (b2b_us[ci] * 1e-6) / 1e9 / hbm_peak,
                   "isolated_us": iso_us[ci], "isolated_gbs": d["bytes"] / (iso_us[ci] * 1e-6) / 1e9}
                  for ci, d in enumerate(cases)]
-    dom = "k_gemv_stream"
+    dom = "k_gemv_decode"  # both forms (k_gemv_decode, k_gemv_decode_tiles) come from gemv.cuh
     launch_bytes = sum(d["bytes"] for d in cases) / ncase
     launch_us = sum(b2b_us) / ncase
     achieved = launch_bytes / (launch_us * 1e-6) / 1e9
@@ -411,7 +413,7 @@ def run_ours(args, world, rank, local):
         for ci, d in enumerate(cases):
             c = d["c"]
             Wq, sw, Wd = d["reps"][(i * ncase + ci) % R]
-            api.llmint8_matmul_host(hX[ci], d["Xd"], c.threshold, Wq, sw, None, Wd, d["Y"], hY[ci], d["ws"])
+            api.llmint8_matmul_host(hX[ci], d["Xd"], c.threshold, Wq, sw, Wd, d["Y"], hY[ci], d["ws"])
 
     def timed(fn, n):
         for i in range(args.warmup):
@@ -516,27 +518,27 @@ def run_prefill(args, dev, stream, bf16_peak, peak_src, iters=None):
         W, _ = c.w()
         Xd = torch.from_numpy(X).to(dev)
         Wd = torch.from_numpy(W).to(dev)
-        Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd)
-        reps = [(Wq, sw, Wq16, Wd), (Wq.clone(), sw.clone(), Wq16.clone(), Wd.clone())]
+        Wq, sw = api.llmint8_quantize_weight(Wd)
+        reps = [(Wq, sw, Wd), (Wq.clone(), sw.clone(), Wd.clone())]
         ws = api.make_workspace(c.M, c.K, c.N, dev)
         Y = torch.empty((c.M, c.N), dtype=torch.float16, device=dev)
         e0 = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
         e1 = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
 
         def call(i, timed):  # the public call, as a user runs it
-            Wq_, sw_, Wq16_, Wd_ = reps[i % 2]
+            Wq_, sw_, Wd_ = reps[i % 2]
             if timed:
                 e0[i].record(stream)
-            api.llmint8_matmul(Xd, c.threshold, Wq_, sw_, Wq16_, Wd_, Y=Y, workspace=ws, stream=stream)
+            api.llmint8_matmul(Xd, c.threshold, Wq_, sw_, Wd_, Y=Y, workspace=ws, stream=stream)
             if timed:
                 e1[i].record(stream)
 
         def split(i, timed):  # its two halves, with events around the GEMM stage
-            Wq_, sw_, Wq16_, Wd_ = reps[i % 2]
+            Wq_, sw_, Wd_ = reps[i % 2]
             api.llmint8_xpass(Xd, c.threshold, c.N, ws, stream=stream)
             if timed:
                 e0[i].record(stream)
-            api.llmint8_gemm(Xd, c.threshold, Wq_, sw_, Wq16_, Wd_, Y, ws, stream=stream)
+            api.llmint8_gemm(Xd, c.threshold, Wq_, sw_, Wd_, Y, ws, stream=stream)
             if timed:
                 e1[i].record(stream)
 
@@ -558,7 +560,7 @@ def run_prefill(args, dev, stream, bf16_peak, peak_src, iters=None):
         tot_flop += flop
         tot_call_ms += call_ms
         tot_gemm_ms += gemm_ms
-        del reps, Wq, sw, Wq16, Wd, Xd, ws, Y
+        del reps, Wq, sw, Wd, Xd, ws, Y
     torch.cuda.empty_cache()
     tops = tot_flop / (tot_call_ms * 1e-3) / 1e12
     tops_gemm = tot_flop / (tot_gemm_ms * 1e-3) / 1e12
@@ -566,6 +568,7 @@ def run_prefill(args, dev, stream, bf16_peak, peak_src, iters=None):
             "value": tops, "unit": "TOPS", "iters": iters,
             "roofline": {"bound": "tensor", "achieved": tops_gemm, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": tops_gemm / bf16_peak, "kernel": "k_gemm_tc",
+                         "stage": "llmint8_gemm: k_widen_codes (int8 codes -> fp16 scratch) then k_gemm_tc",
                          "peak_source": f"{peak_src} bf16_tflops (cuBLAS, burst); tcgen05 kind::f16 runs at the "
                                         "bf16 rate; sm_103a has no int8 tcgen05 kind"},
             "shapes": out}
@@ -605,10 +608,10 @@ def run_sweep(args, dev, stream, hbm_peak, bf16_peak, peak_src):
         W, _ = cs[0].w()
         Wd = torch.from_numpy(W).to(dev)
         del W
-        Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd)
+        Wq, sw = api.llmint8_quantize_weight(Wd)
         R2 = max(2, -(-3 * L2_BYTES // (K * N)))  # replicas: >= 3 x L2 of int8 weights between re-reads
         R2 = min(R2, 4)
-        reps = [(Wq, sw, Wq16, Wd)] + [(Wq.clone(), sw.clone(), Wq16.clone(), Wd.clone()) for _ in range(R2 - 1)]
+        reps = [(Wq, sw, Wd)] + [(Wq.clone(), sw.clone(), Wd.clone()) for _ in range(R2 - 1)]
         for c in cs:
             key = (c.M, K, c.frac, c.mag)
             if key not in xcache:
@@ -622,8 +625,8 @@ def run_sweep(args, dev, stream, hbm_peak, bf16_peak, peak_src):
             dec = M <= 16
 
             def call(i, t=c.threshold):
-                Wq_, sw_, Wq16_, Wd_ = reps[i % R2]
-                api.llmint8_matmul(Xd, t, Wq_, sw_, None if dec else Wq16_, Wd_, Y=Y, workspace=ws, stream=stream)
+                Wq_, sw_, Wd_ = reps[i % R2]
+                api.llmint8_matmul(Xd, t, Wq_, sw_, Wd_, Y=Y, workspace=ws, stream=stream)
 
             us = timed(call, n)
             n_o = api.read_intermediates(ws, M, K, N)["outlier_count"]
@@ -632,7 +635,7 @@ def run_sweep(args, dev, stream, hbm_peak, bf16_peak, peak_src):
                    "tops": flop / (us * 1e-6) / 1e12}
             if dec:
                 gbs = alg_bytes(M, K, N, n_o) / (us * 1e-6) / 1e9
-                row.update(gbs=gbs, bound="hbm", frac=gbs / hbm_peak, kernel="k_gemv_stream")
+                row.update(gbs=gbs, bound="hbm", frac=gbs / hbm_peak, kernel="k_gemv_decode")
             else:
                 row.update(bound="tensor", frac=row["tops"] / bf16_peak, kernel="k_gemm_tc")
             if c.frac == 0.001 or (c.frac == 0.01 and K != 8192):
@@ -641,7 +644,7 @@ def run_sweep(args, dev, stream, hbm_peak, bf16_peak, peak_src):
                 row["fp16_cublas_us"] = timed(lambda i: torch.matmul(Xd, reps[i % R2][3], out=Y), n)
             rows.append(row)
             del ws, Y
-        del reps, Wq, sw, Wq16, Wd
+        del reps, Wq, sw, Wd
         xcache.clear()
         torch.cuda.empty_cache()
     return {"workloads": ["13B-like FFN: M=4096, (K,N) in {(5120,13824),(13824,5120)}; 1% outlier columns "
@@ -679,7 +682,7 @@ def run_chain(args, dev, stream, steps=None):
                 W, _ = synthetic.make_w(K, N, sigma=1.0 / math.sqrt(K), boosted_frac=0.001, boost=10.0,
                                         seed=7000 + li)
             Wd = torch.from_numpy(W).to(dev)
-            Wq, sw, _ = api.llmint8_quantize_weight(Wd, fp16_codes=False)
+            Wq, sw = api.llmint8_quantize_weight(Wd)
             wts.append([(Wq, sw, Wd)] + [(Wq.clone(), sw.clone(), Wd.clone()) for _ in range(R - 1)])
         return wts
 
@@ -707,7 +710,7 @@ def run_chain(args, dev, stream, steps=None):
                 x = X0
                 for li in range(len(layers)):
                     Wq, sw, Wd = wts[li][r % R]
-                    api.llmint8_matmul(x, t, Wq, sw, None, Wd, Y=Ys[li], workspace=wss[li])
+                    api.llmint8_matmul(x, t, Wq, sw, Wd, Y=Ys[li], workspace=wss[li])
                     x = Ys[li]
 
             res = {}
@@ -774,17 +777,16 @@ def run_ablation(args):
         X, _ = synthetic.make_x(M, K, frac=frac, min_count=4 if frac > 0 else 0, seed=M + K + N)
         W, _ = synthetic.make_w(K, N, sigma=0.015 if K == 8192 else 0.02, seed=M + K + N)
         Xd, Wd = torch.from_numpy(X).to(dev), torch.from_numpy(W).to(dev)
-        Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd, fp16_codes=M > 16)
-        reps = [(Wq, sw, Wq16, Wd)] + [(Wq.clone(), sw.clone(), None if Wq16 is None else Wq16.clone(), Wd.clone())
-                                       for _ in range(R - 1)]
+        Wq, sw = api.llmint8_quantize_weight(Wd)
+        reps = [(Wq, sw, Wd)] + [(Wq.clone(), sw.clone(), Wd.clone()) for _ in range(R - 1)]
         ws = api.make_workspace(M, K, N, dev)
         exact = Xd.double() @ Wd.double()
         variants = {
-            "llmint8_t6": lambda r: api.llmint8_matmul(Xd, 6.0, r[0], r[1], r[2], r[3], workspace=ws),
+            "llmint8_t6": lambda r: api.llmint8_matmul(Xd, 6.0, r[0], r[1], r[2], workspace=ws),
             # no fp16 copy of W kept: the outlier rows come from the dequantized codes
-            "llmint8_t6_int8_weights": lambda r: api.llmint8_matmul_w8(Xd, 6.0, r[0], r[1], r[2], workspace=ws),
-            "int8_no_outliers": lambda r: api.llmint8_matmul_int8(Xd, r[0], r[1], r[2], workspace=ws),
-            "fp16_cublas": lambda r: torch.matmul(Xd, r[3]),
+            "llmint8_t6_int8_weights": lambda r: api.llmint8_matmul_w8(Xd, 6.0, r[0], r[1], workspace=ws),
+            "int8_no_outliers": lambda r: api.llmint8_matmul_int8(Xd, r[0], r[1], workspace=ws),
+            "fp16_cublas": lambda r: torch.matmul(Xd, r[2]),
         }
         row = {"case": name, "M": M, "K": K, "N": N, "outlier_frac": frac}
         for key, fn in variants.items():
@@ -803,7 +805,7 @@ def run_ablation(args):
             torch.cuda.synchronize()
             row[key] = {"rel_error": err, "us": 1e3 * e0.elapsed_time(e1) / 20}
         rows.append(row)
-        del Xd, Wd, Wq, sw, Wq16, reps, ws, exact
+        del Xd, Wd, Wq, sw, reps, ws, exact
         torch.cuda.empty_cache()
     print(json.dumps({"ablation": rows, "data": "synthetic", "note": (
         "per-tensor scales change only the scale arrays, not the kernels' work, so their speed is the "
@@ -823,16 +825,16 @@ def run_profile(args):
     W, _ = c.w()
     dev = torch.device("cuda")
     Xd, Wd = torch.from_numpy(X).to(dev), torch.from_numpy(W).to(dev)
-    Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd, fp16_codes=c.M > 16)
+    Wq, sw = api.llmint8_quantize_weight(Wd)
     ws = api.make_workspace(c.M, c.K, c.N, dev)
     Y = torch.empty((c.M, c.N), dtype=torch.float16, device=dev)
     for _ in range(args.warmup):
-        api.llmint8_matmul(Xd, c.threshold, Wq, sw, Wq16, Wd, Y=Y, workspace=ws)
+        api.llmint8_matmul(Xd, c.threshold, Wq, sw, Wd, Y=Y, workspace=ws)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
-        api.llmint8_matmul(Xd, c.threshold, Wq, sw, Wq16, Wd, Y=Y, workspace=ws)
+        api.llmint8_matmul(Xd, c.threshold, Wq, sw, Wd, Y=Y, workspace=ws)
     e1.record()
     torch.cuda.synchronize()
     st = api.llmint8_device_status(ws)

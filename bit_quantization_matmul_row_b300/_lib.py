@@ -61,21 +61,21 @@ def load() -> ctypes.CDLL:
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.llmint8_status_str.argtypes = [I]
         lib.llmint8_status_str.restype = ctypes.c_char_p
-        lib.llmint8_quantize_weight.argtypes = [P, I, I, P, P, P, P]
+        lib.llmint8_quantize_weight.argtypes = [P, I, I, P, P, P]
         lib.llmint8_workspace_bytes.argtypes = [I, I, I]
         lib.llmint8_workspace_bytes.restype = Z
-        lib.llmint8_matmul.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
-        lib.llmint8_matmul_host.argtypes = [P, P, I, I, I, F, P, P, P, P, P, P, P, Z, P]
-        lib.llmint8_matmul_int8.argtypes = [P, I, I, I, P, P, P, P, P, Z, P]
-        lib.llmint8_matmul_w8.argtypes = [P, I, I, I, F, P, P, P, P, P, I, P, P, Z, P]
+        lib.llmint8_matmul.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
+        lib.llmint8_matmul_host.argtypes = [P, P, I, I, I, F, P, P, P, P, P, P, Z, P]
+        lib.llmint8_matmul_int8.argtypes = [P, I, I, I, P, P, P, P, Z, P]
+        lib.llmint8_matmul_w8.argtypes = [P, I, I, I, F, P, P, P, P, I, P, P, Z, P]
         lib.llmint8_pack_w16_rows.argtypes = [P, I, I, P, I, P, P, P]
-        lib.llmint8_quantize_weight_bf16.argtypes = [P, I, I, P, P, P, P]
-        lib.llmint8_matmul_bf16.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
-        lib.llmint8_matmul_i32_bf16.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
-        lib.llmint8_matmul_i32.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
+        lib.llmint8_quantize_weight_bf16.argtypes = [P, I, I, P, P, P]
+        lib.llmint8_matmul_bf16.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
+        lib.llmint8_matmul_i32_bf16.argtypes = [P, I, I, I, F, P, P, P, P, Z, P]
+        lib.llmint8_matmul_i32.argtypes = [P, I, I, I, F, P, P, P, P, Z, P]
         lib.llmint8_xpass.argtypes = [P, I, I, I, F, P, Z, P]
-        lib.llmint8_gemm.argtypes = [P, I, I, I, F, P, P, P, P, P, P, Z, P]
-        lib.llmint8_matmul_noalloc.argtypes = [P, I, I, I, F, P, P, P, P, P, P]
+        lib.llmint8_gemm.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
+        lib.llmint8_matmul_noalloc.argtypes = [P, I, I, I, F, P, P, P, P, P]
         lib.llmint8_chain_state_bytes.argtypes = [I, I]
         lib.llmint8_chain_state_bytes.restype = Z
         lib.llmint8_chain_state_layout.argtypes = [I, I, ctypes.POINTER(Z)]

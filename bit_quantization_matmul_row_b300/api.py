@@ -77,45 +77,37 @@ def make_workspace(M: int, K: int, N: int, device=None) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def llmint8_quantize_weight(W: torch.Tensor, Wq=None, colScaleW=None, Wq16=None, fp16_codes: bool = True,
-                            stream=None):
-    """A0: W fp16 [K, N] -> (Wq int8 [N, K], colScaleW fp32 [N], Wq16 fp16 [N, K] or None)."""
+def llmint8_quantize_weight(W: torch.Tensor, Wq=None, colScaleW=None, stream=None):
+    """A0: W fp16 [K, N] -> (Wq int8 [N, K], colScaleW fp32 [N])."""
     K, N = W.shape
     dev = W.device
     if Wq is None:
         Wq = torch.empty((N, K), dtype=torch.int8, device=dev)
     if colScaleW is None:
         colScaleW = torch.empty((N,), dtype=torch.float32, device=dev)
-    if Wq16 is None and fp16_codes:
-        Wq16 = torch.empty((N, K), dtype=torch.float16, device=dev)
     _need(W, torch.float16, (K, N), "W")
     _need(Wq, torch.int8, (N, K), "Wq")
     _need(colScaleW, torch.float32, (N,), "colScaleW")
-    _need(Wq16, torch.float16, (N, K), "Wq16")
-    st = _lib.load().llmint8_quantize_weight(_ptr(W), K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Wq16), _stream(stream, W))
+    st = _lib.load().llmint8_quantize_weight(_ptr(W), K, N, _ptr(Wq), _ptr(colScaleW), _stream(stream, W))
     _check(st, "llmint8_quantize_weight")
-    return Wq, colScaleW, Wq16
+    return Wq, colScaleW
 
 
-def llmint8_quantize_weight_bf16(W: torch.Tensor, Wq=None, colScaleW=None, Wq16=None, fp16_codes: bool = True,
-                                 stream=None):
-    """A0 for bf16 W [K, N] -> (Wq int8 [N, K], colScaleW fp32 [N], Wq16 fp16 codes [N, K] or None)."""
+def llmint8_quantize_weight_bf16(W: torch.Tensor, Wq=None, colScaleW=None, stream=None):
+    """A0 for bf16 W [K, N] -> (Wq int8 [N, K], colScaleW fp32 [N])."""
     K, N = W.shape
     dev = W.device
     if Wq is None:
         Wq = torch.empty((N, K), dtype=torch.int8, device=dev)
     if colScaleW is None:
         colScaleW = torch.empty((N,), dtype=torch.float32, device=dev)
-    if Wq16 is None and fp16_codes:
-        Wq16 = torch.empty((N, K), dtype=torch.float16, device=dev)
     _need(W, torch.bfloat16, (K, N), "W")
     _need(Wq, torch.int8, (N, K), "Wq")
     _need(colScaleW, torch.float32, (N,), "colScaleW")
-    _need(Wq16, torch.float16, (N, K), "Wq16")
-    st = _lib.load().llmint8_quantize_weight_bf16(_ptr(W), K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
+    st = _lib.load().llmint8_quantize_weight_bf16(_ptr(W), K, N, _ptr(Wq), _ptr(colScaleW),
                                                   _stream(stream, W))
     _check(st, "llmint8_quantize_weight_bf16")
-    return Wq, colScaleW, Wq16
+    return Wq, colScaleW
 
 
 def _shapes(X, Wq):
@@ -124,7 +116,7 @@ def _shapes(X, Wq):
     return M, K, N
 
 
-def llmint8_matmul(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspace=None, stream=None):
+def llmint8_matmul(X, threshold, Wq, colScaleW, W16, Y=None, workspace=None, stream=None):
     """A1..A5: Y = X.W with the LLM.int8() decomposition at `threshold`."""
     M, K, N = _shapes(X, Wq)
     if Y is None:
@@ -133,13 +125,13 @@ def llmint8_matmul(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspace=Non
         workspace = make_workspace(M, K, N, X.device)
     _need(X, torch.float16, (M, K), "X")
     _need(Y, torch.float16, (M, N), "Y")
-    st = _lib.load().llmint8_matmul(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
-                                    _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream, X))
+    st = _lib.load().llmint8_matmul(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(W16),
+                                    _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul")
     return Y
 
 
-def llmint8_matmul_host(X_host, X, threshold, Wq, colScaleW, Wq16, W16, Y, Y_host, workspace, stream=None):
+def llmint8_matmul_host(X_host, X, threshold, Wq, colScaleW, W16, Y, Y_host, workspace, stream=None):
     """llmint8_matmul between host tensors: X_host -> X (device), Y = X.W, Y -> Y_host, all
     enqueued on the stream by one call (synchronize before reading Y_host)."""
     M, K, N = _shapes(X, Wq)
@@ -150,7 +142,7 @@ def llmint8_matmul_host(X_host, X, threshold, Wq, colScaleW, Wq16, W16, Y, Y_hos
     if X_host.is_cuda or Y_host.is_cuda or not X.is_cuda:
         raise ValueError("llmint8_matmul_host: X_host and Y_host are host tensors, X and Y device tensors")
     st = _lib.load().llmint8_matmul_host(_ptr(X_host), _ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW),
-                                         _ptr(Wq16), _ptr(W16), _ptr(Y), _ptr(Y_host), _ptr(workspace),
+                                         _ptr(W16), _ptr(Y), _ptr(Y_host), _ptr(workspace),
                                          workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul_host")
     return Y_host
@@ -255,7 +247,7 @@ def llmint8_pack_w16_rows(W16, rows, stream=None):
     return W16c, row_map
 
 
-def llmint8_matmul_w8(X, threshold, Wq, colScaleW, Wq16, W16c=None, row_map=None, Y=None, workspace=None,
+def llmint8_matmul_w8(X, threshold, Wq, colScaleW, W16c=None, row_map=None, Y=None, workspace=None,
                       stream=None):
     """A1..A5 without a full fp16 copy of W: outlier rows from W16c via row_map, else dequantized codes."""
     M, K, N = _shapes(X, Wq)
@@ -268,14 +260,14 @@ def llmint8_matmul_w8(X, threshold, Wq, colScaleW, Wq16, W16c=None, row_map=None
     _need(row_map, torch.int32, (K,), "row_map")
     R = 0 if W16c is None else W16c.shape[0]
     _need(W16c, torch.float16, (R, N), "W16c")
-    st = _lib.load().llmint8_matmul_w8(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
+    st = _lib.load().llmint8_matmul_w8(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW),
                                        _ptr(W16c) if R else None, _ptr(row_map), R, _ptr(Y), _ptr(workspace),
                                        workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul_w8")
     return Y
 
 
-def llmint8_matmul_bf16(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspace=None, stream=None):
+def llmint8_matmul_bf16(X, threshold, Wq, colScaleW, W16, Y=None, workspace=None, stream=None):
     """A1..A5 on bf16 X [M, K] and W16 [K, N] -> Y bf16 [M, N]."""
     M, K, N = _shapes(X, Wq)
     if Y is None:
@@ -285,13 +277,13 @@ def llmint8_matmul_bf16(X, threshold, Wq, colScaleW, Wq16, W16, Y=None, workspac
     _need(X, torch.bfloat16, (M, K), "X")
     _need(Y, torch.bfloat16, (M, N), "Y")
     _need(W16, torch.bfloat16, (K, N), "W16")
-    st = _lib.load().llmint8_matmul_bf16(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
-                                         _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream, X))
+    st = _lib.load().llmint8_matmul_bf16(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(W16),
+                                         _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul_bf16")
     return Y
 
 
-def llmint8_matmul_i32_bf16(X, threshold, Wq, colScaleW, Wq16, C=None, workspace=None, stream=None):
+def llmint8_matmul_i32_bf16(X, threshold, Wq, colScaleW, C=None, workspace=None, stream=None):
     """The exact int32 accumulator C of llmint8_matmul_bf16 (bf16 X)."""
     M, K, N = _shapes(X, Wq)
     if C is None:
@@ -301,13 +293,13 @@ def llmint8_matmul_i32_bf16(X, threshold, Wq, colScaleW, Wq16, C=None, workspace
     _need(X, torch.bfloat16, (M, K), "X")
     _need(C, torch.int32, (M, N), "C")
     st = _lib.load().llmint8_matmul_i32_bf16(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW),
-                                             _ptr(Wq16), _ptr(C), _ptr(workspace), workspace.numel(),
+                                             _ptr(C), _ptr(workspace), workspace.numel(),
                                              _stream(stream, X))
     _check(st, "llmint8_matmul_i32_bf16")
     return C
 
 
-def llmint8_matmul_int8(X, Wq, colScaleW, Wq16, Y=None, workspace=None, stream=None):
+def llmint8_matmul_int8(X, Wq, colScaleW, Y=None, workspace=None, stream=None):
     """Plain vector-wise int8 (threshold = +inf, no fp16 weight)."""
     M, K, N = _shapes(X, Wq)
     if Y is None:
@@ -316,13 +308,13 @@ def llmint8_matmul_int8(X, Wq, colScaleW, Wq16, Y=None, workspace=None, stream=N
         workspace = make_workspace(M, K, N, X.device)
     _need(X, torch.float16, (M, K), "X")
     _need(Y, torch.float16, (M, N), "Y")
-    st = _lib.load().llmint8_matmul_int8(_ptr(X), M, K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Wq16), _ptr(Y),
+    st = _lib.load().llmint8_matmul_int8(_ptr(X), M, K, N, _ptr(Wq), _ptr(colScaleW), _ptr(Y),
                                          _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul_int8")
     return Y
 
 
-def llmint8_matmul_i32(X, threshold, Wq, colScaleW, Wq16, C=None, workspace=None, stream=None):
+def llmint8_matmul_i32(X, threshold, Wq, colScaleW, C=None, workspace=None, stream=None):
     """Same path, but returns the exact int32 accumulator C = Xq . Wq^T of step A3."""
     M, K, N = _shapes(X, Wq)
     if C is None:
@@ -331,8 +323,8 @@ def llmint8_matmul_i32(X, threshold, Wq, colScaleW, Wq16, C=None, workspace=None
         workspace = make_workspace(M, K, N, X.device)
     _need(X, torch.float16, (M, K), "X")
     _need(C, torch.int32, (M, N), "C")
-    st = _lib.load().llmint8_matmul_i32(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
-                                        _ptr(C), _ptr(workspace), workspace.numel(), _stream(stream, X))
+    st = _lib.load().llmint8_matmul_i32(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(C),
+                                        _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_matmul_i32")
     return C
 
@@ -346,12 +338,12 @@ def llmint8_xpass(X, threshold, N, workspace, stream=None):
     _check(st, "llmint8_xpass")
 
 
-def llmint8_gemm(X, threshold, Wq, colScaleW, Wq16, W16, Y, workspace, stream=None):
+def llmint8_gemm(X, threshold, Wq, colScaleW, W16, Y, workspace, stream=None):
     """A3..A5 from a workspace filled by llmint8_xpass (second half of llmint8_matmul)."""
     M, K, N = _shapes(X, Wq)
     _need(Y, torch.float16, (M, N), "Y")
-    st = _lib.load().llmint8_gemm(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(Wq16),
-                                  _ptr(W16), _ptr(Y), _ptr(workspace), workspace.numel(), _stream(stream, X))
+    st = _lib.load().llmint8_gemm(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW), _ptr(W16), _ptr(Y),
+                                  _ptr(workspace), workspace.numel(), _stream(stream, X))
     _check(st, "llmint8_gemm")
     return Y
 
@@ -359,7 +351,7 @@ def llmint8_gemm(X, threshold, Wq, colScaleW, Wq16, W16, Y, workspace, stream=No
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
-def llmint8_matmul_noalloc(X, threshold, Wq, colScaleW, Wq16, W16, Y, stream=None):
+def llmint8_matmul_noalloc(X, threshold, Wq, colScaleW, W16, Y, stream=None):
     """llmint8_matmul on the library's static scratch array (no workspace, no allocation).
 
     Y must be passed in: this call allocates nothing, not even through torch.
@@ -368,7 +360,7 @@ def llmint8_matmul_noalloc(X, threshold, Wq, colScaleW, Wq16, W16, Y, stream=Non
     _need(X, torch.float16, (M, K), "X")
     _need(Y, torch.float16, (M, N), "Y")
     st = _lib.load().llmint8_matmul_noalloc(_ptr(X), M, K, N, float(threshold), _ptr(Wq), _ptr(colScaleW),
-                                            _ptr(Wq16), _ptr(W16), _ptr(Y), _stream(stream, X))
+                                            _ptr(W16), _ptr(Y), _stream(stream, X))
     _check(st, "llmint8_matmul_noalloc")
     return Y
 

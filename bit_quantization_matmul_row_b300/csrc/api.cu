@@ -102,7 +102,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Layout {
-    size_t hdr, bitmap, idx, row_scale, codes, xo, w16o, total;
+    size_t hdr, bitmap, idx, row_scale, codes, xo, w16o, wq16, total;
     int kp;  // padded pitch of the gathered outlier operands (multiple of 64)
     bool decode;
 };
@@ -126,6 +126,9 @@ Layout make_layout(int M, int K, int N) {
     off = align_up(off + (size_t)M * L.kp * 2, 256);
     L.w16o = off;
     if (!L.decode) off = align_up(off + (size_t)N * L.kp * 2, 256);
+    // prefill: the weight codes as fp16 integers, [N, K] (the GEMM's B operand)
+    L.wq16 = align_up(off, 1024);
+    if (!L.decode) off = L.wq16 + (size_t)N * K * 2;
     L.total = off;
     return L;
 }
@@ -217,17 +220,15 @@ struct W16Src {
 };
 
 // Checks of the GEMM operands.
-llmint8_status check_operands(int M, float threshold, const int8_t* Wq, const float* colScaleW, const void* Wq16,
-                              const void* W16, const void* out, bool write_i32, const W16Src& src = W16Src()) {
+llmint8_status check_operands(int M, float threshold, const int8_t* Wq, const float* colScaleW, const void* W16,
+                              const void* out, bool write_i32, const W16Src& src = W16Src()) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
-    const bool decode = M <= LLMINT8_DECODE_MAX_M;
+    (void)M;
     if (!Wq || !colScaleW || !out) return LLMINT8_EINVAL;
     if (use_outliers && !W16 && !write_i32 && !src.w8) return LLMINT8_EINVAL;
     if (src.w8 && (src.rows < 0 || (src.rows > 0 && (!src.W16c || !src.row_map)))) return LLMINT8_EINVAL;
     if (src.w8 && src.W16c && !aligned16(src.W16c)) return LLMINT8_EALIGN;
-    if (!decode && !Wq16) return LLMINT8_EINVAL;
-    if (!aligned16(Wq) || !aligned16(colScaleW) || !aligned16(out) || (Wq16 && !aligned16(Wq16)) ||
-        (W16 && !aligned16(W16)))
+    if (!aligned16(Wq) || !aligned16(colScaleW) || !aligned16(out) || (W16 && !aligned16(W16)))
         return LLMINT8_EALIGN;
     return LLMINT8_OK;
 }
@@ -240,6 +241,7 @@ struct WsView {
     __half* codes;
     __half* xo;
     __half* w16o;
+    __half* wq16;
     WsView(void* workspace, const Layout& L) {
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         hdr = reinterpret_cast<WsHeader*>(ws + L.hdr);
@@ -249,6 +251,7 @@ struct WsView {
         codes = reinterpret_cast<__half*>(ws + L.codes);
         xo = reinterpret_cast<__half*>(ws + L.xo);
         w16o = reinterpret_cast<__half*>(ws + L.w16o);
+        wq16 = reinterpret_cast<__half*>(ws + L.wq16);
     }
 };
 
@@ -357,7 +360,7 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
 // A3 + A4 + A5 from the workspace an xpass_launch of the same problem filled.
 template <typename T>
 llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
-                           const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
+                           const float* colScaleW, const void* W16, void* out, bool write_i32,
                            void* workspace, const Layout& L, DeviceInfo* dev, cudaStream_t s,
                            bool w16o_ready = false, const W16Src& src = W16Src()) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
@@ -433,6 +436,14 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
                     (const int32_t*)w.idx, w.w16o, L.kp, w8);
         if (st != LLMINT8_OK) return st;
     }
+    // A3 operand: the int8 codes widened to exact fp16 integers in the scratch
+    {
+        const size_t n16 = (size_t)N * K / 16;
+        const size_t want = (n16 + 256 * kWidenUnroll - 1) / (256 * kWidenUnroll);
+        const size_t cap = (size_t)dev->sms * 8;
+        st = launch(k_widen_codes, dim3((unsigned)(want < cap ? want : cap)), dim3(256), 0, s, true, Wq, w.wq16, n16);
+        if (st != LLMINT8_OK) return st;
+    }
     if ((st = get_encoder()) != LLMINT8_OK) return st;
     // CTA pairs (256 x 256 tiles, each CTA loading 128 columns of B) once M
     // spans two 128-row tiles; 256 x 128 pair tiles when the wide ones would
@@ -444,7 +455,7 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
     const int b_rows = pair ? bn / 2 : bn;
     CUtensorMap tm_a, tm_b, tm_xo, tm_wo;
     if ((st = encode_fp16_2d(&tm_a, w.codes, M, K, K, kBM)) != LLMINT8_OK) return st;
-    if ((st = encode_fp16_2d(&tm_b, Wq16, N, K, K, b_rows)) != LLMINT8_OK) return st;
+    if ((st = encode_fp16_2d(&tm_b, w.wq16, N, K, K, b_rows)) != LLMINT8_OK) return st;
     if ((st = encode_fp16_2d(&tm_xo, w.xo, M, L.kp, L.kp, kBM)) != LLMINT8_OK) return st;
     if ((st = encode_fp16_2d(&tm_wo, w.w16o, N, L.kp, L.kp, b_rows)) != LLMINT8_OK) return st;
     {
@@ -513,19 +524,21 @@ int kernels_per_call(int M, int K, int N, float threshold, bool write_i32) {
     int n = (scan ? 1 : 0) + 1 + 1;  // scan, row quant, GEMV / GEMM
     // outlier rows of W16 for the GEMM, unless the row quantization gathers them
     if (M > LLMINT8_DECODE_MAX_M && use_outliers && !write_i32 && K > 4096) n += 1;
+    // the codes widened to fp16 for the tensor cores
+    if (M > LLMINT8_DECODE_MAX_M) n += 1;
     (void)N;
     return n;
 }
 
 llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
-                           const float* colScaleW, const void* Wq16, const void* W16, void* out, bool write_i32,
+                           const float* colScaleW, const void* W16, void* out, bool write_i32,
                            void* workspace, size_t ws_bytes, void* stream, const W16Src& src = W16Src(),
                            bool bf16 = false) {
     Layout L;
     DeviceInfo* dev = nullptr;
     llmint8_status st = check_common(X, M, K, N, threshold, workspace, ws_bytes, &L, &dev);
     if (st != LLMINT8_OK) return st;
-    if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, out, write_i32, src)) != LLMINT8_OK) return st;
+    if ((st = check_operands(M, threshold, Wq, colScaleW, W16, out, write_i32, src)) != LLMINT8_OK) return st;
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the row quantization gathers only from a full fp16 copy (W16 is null in w8 mode)
@@ -534,11 +547,11 @@ llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, 
     if (bf16) {
         if ((st = xpass_launch<__nv_bfloat16>(X, M, K, threshold, workspace, L, dev, s, W16, N, gw)) != LLMINT8_OK)
             return st;
-        return gemm_launch<__nv_bfloat16>(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16g, out, write_i32,
+        return gemm_launch<__nv_bfloat16>(X, M, K, N, threshold, Wq, colScaleW, W16g, out, write_i32,
                                           workspace, L, dev, s, gw, src);
     }
     if ((st = xpass_launch<__half>(X, M, K, threshold, workspace, L, dev, s, W16, N, gw)) != LLMINT8_OK) return st;
-    return gemm_launch<__half>(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16g, out, write_i32, workspace, L, dev,
+    return gemm_launch<__half>(X, M, K, N, threshold, Wq, colScaleW, W16g, out, write_i32, workspace, L, dev,
                                s, gw, src);
 }
 
@@ -620,12 +633,11 @@ __global__ void k_selftest_timeout(WsHeader* hdr, uint32_t spin_limit) {
 
 // A0 for W of element format T (fp16 or bf16)
 template <typename T>
-llmint8_status quantize_weight_impl(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* Wq16,
-                                    void* stream) {
+llmint8_status quantize_weight_impl(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* stream) {
     if (!W || !Wq || !colScaleW) return LLMINT8_EINVAL;
     if (K < 1 || N < 1 || K > (1 << 30) || N > (1 << 30)) return LLMINT8_EINVAL;
     if ((K % 16) || (N % 16)) return LLMINT8_EALIGN;
-    if (!aligned16(W) || !aligned16(Wq) || !aligned16(colScaleW) || (Wq16 && !aligned16(Wq16))) return LLMINT8_EALIGN;
+    if (!aligned16(W) || !aligned16(Wq) || !aligned16(colScaleW)) return LLMINT8_EALIGN;
     DeviceInfo* dev = nullptr;
     llmint8_status st = current_device(&dev);
     if (st != LLMINT8_OK) return st;
@@ -639,7 +651,7 @@ llmint8_status quantize_weight_impl(const void* W, int K, int N, int8_t* Wq, flo
     k_col_absmax<T><<<dim3(gx, gy), 256, 0, s>>>(static_cast<const __half*>(W), K, N, colScaleW);
     if ((st = launch_status()) != LLMINT8_OK) return st;
     k_quantize_weight_tile<T><<<dim3((N + 63) / 64, (K + 63) / 64), 256, 0, s>>>(
-        static_cast<const __half*>(W), K, N, colScaleW, Wq, static_cast<__half*>(Wq16));
+        static_cast<const __half*>(W), K, N, colScaleW, Wq);
     return launch_status();
 }
 
@@ -658,27 +670,25 @@ const char* llmint8_status_str(int status) {
     }
 }
 
-llmint8_status llmint8_quantize_weight(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* Wq16,
-                                       void* stream) {
-    return quantize_weight_impl<__half>(W, K, N, Wq, colScaleW, Wq16, stream);
+llmint8_status llmint8_quantize_weight(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* stream) {
+    return quantize_weight_impl<__half>(W, K, N, Wq, colScaleW, stream);
 }
 
-llmint8_status llmint8_quantize_weight_bf16(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* Wq16,
-                                            void* stream) {
-    return quantize_weight_impl<__nv_bfloat16>(W, K, N, Wq, colScaleW, Wq16, stream);
+llmint8_status llmint8_quantize_weight_bf16(const void* W, int K, int N, int8_t* Wq, float* colScaleW, void* stream) {
+    return quantize_weight_impl<__nv_bfloat16>(W, K, N, Wq, colScaleW, stream);
 }
 
 llmint8_status llmint8_matmul_bf16(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
-                                   const float* colScaleW, const void* Wq16, const void* W16, void* Y, void* workspace,
+                                   const float* colScaleW, const void* W16, void* Y, void* workspace,
                                    size_t workspace_bytes, void* stream) {
-    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, workspace_bytes,
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, W16, Y, false, workspace, workspace_bytes,
                        stream, W16Src(), true);
 }
 
 llmint8_status llmint8_matmul_i32_bf16(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
-                                       const float* colScaleW, const void* Wq16, int32_t* C, void* workspace,
+                                       const float* colScaleW, int32_t* C, void* workspace,
                                        size_t workspace_bytes, void* stream) {
-    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, nullptr, C, true, workspace, workspace_bytes,
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, nullptr, C, true, workspace, workspace_bytes,
                        stream, W16Src(), true);
 }
 
@@ -688,14 +698,14 @@ size_t llmint8_workspace_bytes(int M, int K, int N) {
 }
 
 llmint8_status llmint8_matmul(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
-                              const float* colScaleW, const void* Wq16, const void* W16, void* Y, void* workspace,
+                              const float* colScaleW, const void* W16, void* Y, void* workspace,
                               size_t workspace_bytes, void* stream) {
-    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, workspace_bytes,
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, W16, Y, false, workspace, workspace_bytes,
                        stream);
 }
 
 llmint8_status llmint8_matmul_host(const void* X_host, void* X, int M, int K, int N, float threshold,
-                                   const int8_t* Wq, const float* colScaleW, const void* Wq16, const void* W16, void* Y,
+                                   const int8_t* Wq, const float* colScaleW, const void* W16, void* Y,
                                    void* Y_host, void* workspace, size_t workspace_bytes, void* stream) {
     if (!X_host || !Y_host || !Y) return LLMINT8_EINVAL;
     // every argument of the device call is checked before the first copy is enqueued
@@ -703,11 +713,11 @@ llmint8_status llmint8_matmul_host(const void* X_host, void* X, int M, int K, in
     DeviceInfo* dev = nullptr;
     llmint8_status st = check_common(X, M, K, N, threshold, workspace, workspace_bytes, &L, &dev);
     if (st != LLMINT8_OK) return st;
-    if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, Y, false)) != LLMINT8_OK) return st;
+    if ((st = check_operands(M, threshold, Wq, colScaleW, W16, Y, false)) != LLMINT8_OK) return st;
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(X, X_host, (size_t)M * K * 2, cudaMemcpyHostToDevice, s) != cudaSuccess) return LLMINT8_ECUDA;
-    if ((st = llmint8_matmul(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, workspace, workspace_bytes, stream)) !=
+    if ((st = llmint8_matmul(X, M, K, N, threshold, Wq, colScaleW, W16, Y, workspace, workspace_bytes, stream)) !=
         LLMINT8_OK)
         return st;
     return cudaMemcpyAsync(Y_host, Y, (size_t)M * N * 2, cudaMemcpyDeviceToHost, s) == cudaSuccess ? LLMINT8_OK
@@ -715,14 +725,14 @@ llmint8_status llmint8_matmul_host(const void* X_host, void* X, int M, int K, in
 }
 
 llmint8_status llmint8_matmul_w8(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
-                                 const float* colScaleW, const void* Wq16, const void* W16c, const int32_t* row_map,
+                                 const float* colScaleW, const void* W16c, const int32_t* row_map,
                                  int w16_rows, void* Y, void* workspace, size_t workspace_bytes, void* stream) {
     W16Src src;
     src.w8 = true;
     src.W16c = static_cast<const __half*>(W16c);
     src.row_map = row_map;
     src.rows = w16_rows;
-    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, nullptr, Y, false, workspace, workspace_bytes,
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, nullptr, Y, false, workspace, workspace_bytes,
                        stream, src);
 }
 
@@ -747,16 +757,16 @@ llmint8_status llmint8_pack_w16_rows(const void* W16, int K, int N, const int32_
 }
 
 llmint8_status llmint8_matmul_int8(const void* X, int M, int K, int N, const int8_t* Wq, const float* colScaleW,
-                                   const void* Wq16, void* Y, void* workspace, size_t workspace_bytes,
+                                   void* Y, void* workspace, size_t workspace_bytes,
                                    void* stream) {
-    return matmul_impl(X, M, K, N, INFINITY, Wq, colScaleW, Wq16, nullptr, Y, false, workspace, workspace_bytes,
+    return matmul_impl(X, M, K, N, INFINITY, Wq, colScaleW, nullptr, Y, false, workspace, workspace_bytes,
                        stream);
 }
 
 llmint8_status llmint8_matmul_i32(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
-                                  const float* colScaleW, const void* Wq16, int32_t* C, void* workspace,
+                                  const float* colScaleW, int32_t* C, void* workspace,
                                   size_t workspace_bytes, void* stream) {
-    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, Wq16, nullptr, C, true, workspace, workspace_bytes,
+    return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, nullptr, C, true, workspace, workspace_bytes,
                        stream);
 }
 
@@ -809,15 +819,15 @@ llmint8_status llmint8_read_outliers(const void* workspace, int K, int* count, i
 }
 
 llmint8_status llmint8_gemm(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
-                            const float* colScaleW, const void* Wq16, const void* W16, void* Y, void* workspace,
+                            const float* colScaleW, const void* W16, void* Y, void* workspace,
                             size_t workspace_bytes, void* stream) {
     Layout L;
     DeviceInfo* dev = nullptr;
     llmint8_status st = check_common(X, M, K, N, threshold, workspace, workspace_bytes, &L, &dev);
     if (st != LLMINT8_OK) return st;
-    if ((st = check_operands(M, threshold, Wq, colScaleW, Wq16, W16, Y, false)) != LLMINT8_OK) return st;
+    if ((st = check_operands(M, threshold, Wq, colScaleW, W16, Y, false)) != LLMINT8_OK) return st;
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
-    return gemm_launch<__half>(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, false, workspace, L, dev,
+    return gemm_launch<__half>(X, M, K, N, threshold, Wq, colScaleW, W16, Y, false, workspace, L, dev,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -972,8 +982,7 @@ void* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per d
 }  // namespace
 
 extern "C" llmint8_status llmint8_matmul_noalloc(const void* X, int M, int K, int N, float threshold,
-                                                 const int8_t* Wq, const float* colScaleW, const void* Wq16,
-                                                 const void* W16, void* Y, void* stream) {
+                                                 const int8_t* Wq, const float* colScaleW, const void* W16, void* Y, void* stream) {
     if (!sizes_ok(M, K, N)) return LLMINT8_EINVAL;
     if (make_layout(M, K, N).total > kNoAllocScratchBytes) return LLMINT8_EWORKSPACE;
     DeviceInfo* dev = nullptr;
@@ -993,6 +1002,6 @@ extern "C" llmint8_status llmint8_matmul_noalloc(const void* X, int M, int K, in
         }
         scratch = g_noalloc_ptr[d];
     }
-    return llmint8_matmul(X, M, K, N, threshold, Wq, colScaleW, Wq16, W16, Y, scratch, kNoAllocScratchBytes,
+    return llmint8_matmul(X, M, K, N, threshold, Wq, colScaleW, W16, Y, scratch, kNoAllocScratchBytes,
                           stream);
 }

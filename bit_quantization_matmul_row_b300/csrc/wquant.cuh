@@ -4,10 +4,10 @@
 //
 //   colScaleW[n] = max_k |W[k,n]|
 //   Wq[n, k]     = round-half-away(fp32(W[k,n] * fp32(127 / colScaleW[n])))
-//   Wq16[n, k]   = the same code as an exact fp16 value (tensor-core operand)
 //
-// W is [K, N] row-major; the outputs are transposed to [N, K] (K contiguous):
-// the layout both GEMM paths stream.
+// W is [K, N] row-major; Wq is transposed to [N, K] (K contiguous): the layout
+// both product paths stream.  Wq is the only code copy kept: the prefill path
+// widens it into a per-call fp16 scratch (k_widen_codes) for the tensor cores.
 #pragma once
 
 #include "common.cuh"
@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(256) k_col_absmax(const __half* __restrict__ W
 template <typename T>
 __global__ void __launch_bounds__(256) k_quantize_weight_tile(const __half* __restrict__ W, int K, int N,
                                                               const float* __restrict__ col_amax,
-                                                              int8_t* __restrict__ Wq, __half* __restrict__ Wq16) {
+                                                              int8_t* __restrict__ Wq) {
     __shared__ float s_sf[64];
     __shared__ int8_t tile[64][64 + 4];  // [n][k]
     const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
@@ -83,13 +83,46 @@ __global__ void __launch_bounds__(256) k_quantize_weight_tile(const __half* __re
             const uint32_t packed = (uint32_t)(uint8_t)c0 | ((uint32_t)(uint8_t)c1 << 8) |
                                     ((uint32_t)(uint8_t)c2 << 16) | ((uint32_t)(uint8_t)c3 << 24);
             *reinterpret_cast<uint32_t*>(Wq + (size_t)n * K + k) = packed;
-            if (Wq16) {
-                const __half2 h01 = __floats2half2_rn((float)c0, (float)c1);
-                const __half2 h23 = __floats2half2_rn((float)c2, (float)c3);
-                uint2 o;
-                o.x = *reinterpret_cast<const uint32_t*>(&h01);
-                o.y = *reinterpret_cast<const uint32_t*>(&h23);
-                *reinterpret_cast<uint2*>(Wq16 + (size_t)n * K + k) = o;
+        }
+    }
+}
+
+// Prefill operand of A3: the int8 codes Wq [N, K] as exact fp16 integers in a
+// per-call scratch of the same layout, which the tensor-core GEMM loads by TMA
+// (sm_103a has no int8 tcgen05 MMA; kind::f16 on exact integer codes stands in).
+// Each thread widens kWidenUnroll 16-code chunks per step (all loads issued
+// before the stores, grid-strided so that a warp touches 512 contiguous bytes).
+// The scratch is in the workspace, which the previous call's GEMM may still be
+// reading: the stores wait for the predecessor (programmatic dependent launch).
+constexpr int kWidenUnroll = 4;
+__global__ void __launch_bounds__(256, 8) k_widen_codes(const int8_t* __restrict__ Wq, __half* __restrict__ out,
+                                                     size_t n16) {
+    pdl_trigger();
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    bool waited = false;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += kWidenUnroll * stride) {
+        uint4 v[kWidenUnroll];
+#pragma unroll
+        for (int u = 0; u < kWidenUnroll; ++u) {
+            const size_t c = i + u * stride;
+            v[u] = c < n16 ? ldg_nc_v4(Wq + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (!waited) {
+            pdl_wait();
+            waited = true;
+        }
+#pragma unroll
+        for (int u = 0; u < kWidenUnroll; ++u) {
+            const size_t c = i + u * stride;
+            if (c < n16) {
+                uint32_t h[8];
+                s8x4_to_half2x2(v[u].x, h[0], h[1]);
+                s8x4_to_half2x2(v[u].y, h[2], h[3]);
+                s8x4_to_half2x2(v[u].z, h[4], h[5]);
+                s8x4_to_half2x2(v[u].w, h[6], h[7]);
+                uint4* o = reinterpret_cast<uint4*>(out + c * 16);
+                o[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                o[1] = make_uint4(h[4], h[5], h[6], h[7]);
             }
         }
     }

@@ -69,17 +69,21 @@ const char *llmint8_status_str(int status);
  *   Wq        out  int8 [N, K] row-major, i.e. K contiguous per output column:
  *                  Wq[n*K + k] = round-half-away(W[k,n] * fp32(127 / colScaleW[n]))
  *   colScaleW out  fp32 [N], colScaleW[n] = max_k |W[k, n]| over ALL K rows
- *   Wq16      out  optional (may be NULL): fp16 [N, K], the same codes as fp16
- *                  values (exact), the operand layout of the tensor-core GEMM.
- *                  Required by llmint8_matmul* when M > LLMINT8_DECODE_MAX_M.
  *
  * Source: paper walkthrough, section 2.1 (per-column weight scale); Lightning
  * Fabric 8-bit page, section 2.2 (one scale per output channel).
  */
 llmint8_status llmint8_quantize_weight(const void *W, int K, int N, int8_t *Wq, float *colScaleW,
-                                       void *Wq16, void *stream);
+                                       void *stream);
 
-/* Bytes of device workspace llmint8_matmul* needs for this shape (16-byte multiple). */
+/*
+ * Bytes of device workspace llmint8_matmul* needs for this shape (16-byte
+ * multiple).  For M > LLMINT8_DECODE_MAX_M it includes a per-call fp16 copy of
+ * the weight codes (2*N*K bytes): sm_103a has no int8 tcgen05 MMA, so the
+ * prefill path widens Wq into exact fp16 integers there, right before its
+ * tensor-core GEMM (one bandwidth-bound kernel), and the persistent weight
+ * storage stays Wq plus colScaleW (N*K + 4*N bytes).
+ */
 size_t llmint8_workspace_bytes(int M, int K, int N);
 
 /*
@@ -90,8 +94,6 @@ size_t llmint8_workspace_bytes(int M, int K, int N);
  *                   the decomposition (pure vector-wise int8); 0 or a negative
  *                   value makes every nonzero column an outlier; NaN -> EINVAL.
  *   Wq, colScaleW   from llmint8_quantize_weight
- *   Wq16       in   fp16 codes from llmint8_quantize_weight; may be NULL only if
- *                   M <= LLMINT8_DECODE_MAX_M
  *   W16        in   the retained fp16 W [K, N]; may be NULL only if threshold is
  *                   +INFINITY
  *   Y          out  fp16 [M, N] row-major
@@ -102,8 +104,8 @@ size_t llmint8_workspace_bytes(int M, int K, int N);
  * Source: paper walkthrough, sections 2.1-2.3; pitfalls guide, sections 3.1-3.3.
  */
 llmint8_status llmint8_matmul(const void *X, int M, int K, int N, float threshold,
-                              const int8_t *Wq, const float *colScaleW, const void *Wq16,
-                              const void *W16, void *Y, void *workspace, size_t workspace_bytes,
+                              const int8_t *Wq, const float *colScaleW, const void *W16, void *Y,
+                              void *workspace, size_t workspace_bytes,
                               void *stream);
 
 /*
@@ -124,9 +126,10 @@ llmint8_status llmint8_matmul(const void *X, int M, int K, int N, float threshol
  * Errors as llmint8_matmul (all checked before the first copy is enqueued);
  * EINVAL also for a NULL X_host, Y_host or Y; ECUDA if a copy cannot be enqueued.
  */
-llmint8_status llmint8_matmul_host(const void *X_host, void *X, int M, int K, int N, float threshold,
-                                   const int8_t *Wq, const float *colScaleW, const void *Wq16,
-                                   const void *W16, void *Y, void *Y_host, void *workspace,
+llmint8_status llmint8_matmul_host(const void *X_host, void *X, int M, int K, int N,
+float threshold,
+                                   const int8_t *Wq, const float *colScaleW, const void *W16,
+                                   void *Y, void *Y_host, void *workspace,
                                    size_t workspace_bytes, void *stream);
 
 /*
@@ -134,18 +137,19 @@ llmint8_status llmint8_matmul_host(const void *X_host, void *X, int M, int K, in
  * fp16 entry points).  The codes, scales, outlier test and the int32 product are
  * computed from the fp32 values of the bf16 inputs exactly as from fp16 ones;
  * the outlier slice multiplies bf16 X and W values with fp32 accumulation and Y
- * is rounded to bf16 (nearest even).  Wq16 stays fp16 (exact integer codes).
+ * is rounded to bf16 (nearest even).
  * llmint8_matmul_i32_bf16 writes the int32 accumulator C, as llmint8_matmul_i32.
  */
-llmint8_status llmint8_quantize_weight_bf16(const void *W, int K, int N, int8_t *Wq, float *colScaleW,
-                                            void *Wq16, void *stream);
+llmint8_status llmint8_quantize_weight_bf16(const void *W, int K, int N, int8_t *Wq,
+float *colScaleW,
+                                            void *stream);
 llmint8_status llmint8_matmul_bf16(const void *X, int M, int K, int N, float threshold,
-                                   const int8_t *Wq, const float *colScaleW, const void *Wq16,
-                                   const void *W16, void *Y, void *workspace, size_t workspace_bytes,
+                                   const int8_t *Wq, const float *colScaleW, const void *W16,
+                                   void *Y, void *workspace, size_t workspace_bytes,
                                    void *stream);
 llmint8_status llmint8_matmul_i32_bf16(const void *X, int M, int K, int N, float threshold,
-                                       const int8_t *Wq, const float *colScaleW, const void *Wq16,
-                                       int32_t *C, void *workspace, size_t workspace_bytes, void *stream);
+                                       const int8_t *Wq, const float *colScaleW, int32_t *C,
+                                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * llmint8_matmul without a full fp16 copy of W (int8 weight storage only).  The
@@ -172,8 +176,8 @@ llmint8_status llmint8_matmul_i32_bf16(const void *X, int M, int K, int N, float
  * page, section 2.2 (one scale per output column).
  */
 llmint8_status llmint8_matmul_w8(const void *X, int M, int K, int N, float threshold,
-                                 const int8_t *Wq, const float *colScaleW, const void *Wq16,
-                                 const void *W16c, const int32_t *row_map, int w16_rows, void *Y,
+                                 const int8_t *Wq, const float *colScaleW, const void *W16c,
+                                 const int32_t *row_map, int w16_rows, void *Y,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -194,7 +198,8 @@ llmint8_status llmint8_matmul_w8(const void *X, int M, int K, int N, float thres
  * or W16 or W16c is not 16-byte aligned; ECUDA if a launch fails.  Asynchronous
  * on `stream`.
  */
-llmint8_status llmint8_pack_w16_rows(const void *W16, int K, int N, const int32_t *rows, int w16_rows,
+llmint8_status llmint8_pack_w16_rows(const void *W16, int K, int N, const int32_t *rows,
+int w16_rows,
                                      void *W16c, int32_t *row_map, void *stream);
 
 /*
@@ -203,7 +208,7 @@ llmint8_status llmint8_pack_w16_rows(const void *W16, int K, int N, const int32_
  * Source: pitfalls guide, section 1 (plain absmax int8, no outlier handling).
  */
 llmint8_status llmint8_matmul_int8(const void *X, int M, int K, int N, const int8_t *Wq,
-                                   const float *colScaleW, const void *Wq16, void *Y,
+                                   const float *colScaleW, void *Y,
                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -220,12 +225,13 @@ llmint8_status llmint8_matmul_int8(const void *X, int M, int K, int N, const int
  * llmint8_gemm -- steps A3, A4 and A5 (pitfalls guide, sections 3.2-3.3):
  *   consumes a workspace that an llmint8_xpass with the same X, M, K, N and
  *   threshold filled earlier on the same stream (undefined otherwise); X is read
- *   again for the outlier values.  Writes Y fp16 [M, N].
+ *   again for the outlier values.  For M > 16 it first widens Wq into the
+ *   workspace's fp16 code scratch.  Writes Y fp16 [M, N].
  */
 llmint8_status llmint8_xpass(const void *X, int M, int K, int N, float threshold, void *workspace,
                              size_t workspace_bytes, void *stream);
 llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold, const int8_t *Wq,
-                            const float *colScaleW, const void *Wq16, const void *W16, void *Y,
+                            const float *colScaleW, const void *W16, void *Y,
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -238,7 +244,8 @@ llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold,
  * Same rules as llmint8_matmul for X, M, K and threshold; EINVAL for a NULL Xq
  * or rowScaleX, EALIGN for one that is not 16-byte aligned.  Asynchronous.
  */
-llmint8_status llmint8_quantize_x(const void *X, int M, int K, float threshold, int8_t *Xq, float *rowScaleX,
+llmint8_status llmint8_quantize_x(const void *X, int M, int K, float threshold, int8_t *Xq,
+float *rowScaleX,
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -252,7 +259,8 @@ llmint8_status llmint8_quantize_x(const void *X, int M, int K, float threshold, 
  * stored count outside [0, K] (a workspace no X pass of this K has filled);
  * ECUDA if synchronization or a copy fails.
  */
-llmint8_status llmint8_read_outliers(const void *workspace, int K, int *count, int32_t *idx_host, int capacity,
+llmint8_status llmint8_read_outliers(const void *workspace, int K, int *count, int32_t *idx_host,
+int capacity,
                                      void *stream);
 
 /*
@@ -274,7 +282,7 @@ llmint8_status llmint8_read_outliers(const void *workspace, int K, int *count, i
  *   state_in        in   chain state of X written by the previous call's
  *                        state_out (same M, N of that call = K here), or NULL:
  *                        then the usual X pass runs first
- *   Wq, colScaleW, W16, Y   as llmint8_matmul (no Wq16: the GEMV reads Wq)
+ *   Wq, colScaleW, W16, Y   as llmint8_matmul
  *   next_threshold  in   threshold the flags of Y are taken for (not NaN)
  *   state_out       out  chain state of Y (llmint8_chain_state_bytes(M, N)
  *                        bytes, 16-byte aligned), or NULL
@@ -301,8 +309,10 @@ llmint8_status llmint8_read_outliers(const void *workspace, int K, int *count, i
  * one.  Asynchronous on `stream`.
  */
 size_t llmint8_chain_state_bytes(int M, int N);
-llmint8_status llmint8_chain_state_layout(int M, int N, size_t *offsets /* [3]: flags, parts, total */);
-llmint8_status llmint8_matmul_chain(const void *X, int M, int K, int N, float threshold, const void *state_in,
+llmint8_status llmint8_chain_state_layout(int M, int N, size_t *offsets /* [3]: flags, parts,
+total */);
+llmint8_status llmint8_matmul_chain(const void *X, int M, int K, int N, float threshold,
+const void *state_in,
                                     size_t state_in_bytes, const int8_t *Wq, const float *colScaleW,
                                     const void *W16, void *Y, float next_threshold, void *state_out,
                                     size_t state_out_bytes, void *workspace, size_t workspace_bytes,
@@ -313,9 +323,12 @@ llmint8_status llmint8_matmul_chain(const void *X, int M, int K, int N, float th
  * kernel derives from a state are then checkable bit for bit).  Same arguments
  * and errors, plus C (16-byte aligned, not NULL).
  */
-llmint8_status llmint8_matmul_chain_i32(const void *X, int M, int K, int N, float threshold, const void *state_in,
-                                        size_t state_in_bytes, const int8_t *Wq, const float *colScaleW,
-                                        const void *W16, void *Y, float next_threshold, void *state_out,
+llmint8_status llmint8_matmul_chain_i32(const void *X, int M, int K, int N, float threshold,
+const void *state_in,
+                                        size_t state_in_bytes, const int8_t *Wq,
+                                        const float *colScaleW,
+                                        const void *W16, void *Y, float next_threshold,
+                                        void *state_out,
                                         size_t state_out_bytes, int32_t *C, void *workspace,
                                         size_t workspace_bytes, void *stream);
 
@@ -342,8 +355,8 @@ llmint8_status llmint8_matmul_chain_i32(const void *X, int M, int K, int N, floa
  *     llmint8_device_status.
  */
 llmint8_status llmint8_matmul_noalloc(const void *X, int M, int K, int N, float threshold,
-                                      const int8_t *Wq, const float *colScaleW, const void *Wq16,
-                                      const void *W16, void *Y, void *stream);
+                                      const int8_t *Wq, const float *colScaleW, const void *W16,
+                                      void *Y, void *stream);
 
 /* ----------------------------------------------------------------------------
  * Introspection (tests and diagnostics; not on the hot path)
@@ -358,8 +371,8 @@ llmint8_status llmint8_matmul_noalloc(const void *X, int M, int K, int N, float 
  * zeroed, and W16 is not needed.
  */
 llmint8_status llmint8_matmul_i32(const void *X, int M, int K, int N, float threshold,
-                                  const int8_t *Wq, const float *colScaleW, const void *Wq16,
-                                  int32_t *C, void *workspace, size_t workspace_bytes,
+                                  const int8_t *Wq, const float *colScaleW, int32_t *C,
+                                  void *workspace, size_t workspace_bytes,
                                   void *stream);
 
 /*
@@ -369,7 +382,8 @@ llmint8_status llmint8_matmul_i32(const void *X, int M, int K, int N, float thre
  * M <= 16 with K <= 4096, where the row-quantization CTAs form one cluster and
  * find the outlier columns themselves), the row quantization, for M > 16 with a
  * finite threshold, write_i32 = 0 and K > 4096 the gather of the outlier rows
- * of W16 (for K <= 4096 the row quantization writes them), and the GEMV or GEMM.
+ * of W16 (for K <= 4096 the row quantization writes them), for M > 16 the
+ * widening of the weight codes to fp16, and the GEMV or GEMM.
  * The bf16 entry points launch the same kernels; llmint8_matmul_w8 launches the
  * gather for every M > 16 with a finite threshold (one more kernel when
  * K <= 4096).  -1 for arguments the call would reject as EINVAL.

@@ -69,11 +69,11 @@ def test_workspace_layout(lib):
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails its checks first
 
 
-def _mm(lib, M=32, K=64, N=64, t=6.0, X=FAKE, Wq=FAKE, sw=FAKE, wq16=FAKE, w16=FAKE, Y=FAKE, ws=FAKE, wsb=None):
+def _mm(lib, M=32, K=64, N=64, t=6.0, X=FAKE, Wq=FAKE, sw=FAKE, w16=FAKE, Y=FAKE, ws=FAKE, wsb=None):
     if wsb is None:
         wsb = 1 << 40
     P = ctypes.c_void_p
-    return lib.llmint8_matmul(P(X), M, K, N, t, P(Wq), P(sw), P(wq16), P(w16), P(Y), P(ws), wsb, None)
+    return lib.llmint8_matmul(P(X), M, K, N, t, P(Wq), P(sw), P(w16), P(Y), P(ws), wsb, None)
 
 
 def test_matmul_argument_errors(lib):
@@ -83,7 +83,7 @@ def test_matmul_argument_errors(lib):
     assert _mm(lib, t=math.nan) == _lib.EINVAL
     assert _mm(lib, X=0) == _lib.EINVAL
     assert _mm(lib, w16=0) == _lib.EINVAL            # finite threshold needs W16
-    assert _mm(lib, wq16=0) == _lib.EINVAL           # M > 16 needs the fp16 codes
+    assert _mm(lib, Wq=0) == _lib.EINVAL
     assert _mm(lib, K=72) == _lib.EALIGN
     assert _mm(lib, N=40) == _lib.EALIGN
     assert _mm(lib, X=FAKE + 8) == _lib.EALIGN
@@ -94,24 +94,24 @@ def test_matmul_argument_errors(lib):
 def test_int8_variant_needs_no_w16(lib):
     P = ctypes.c_void_p
     # argument checks pass up to the workspace check: W16 is not required
-    st = lib.llmint8_matmul_int8(P(FAKE), 32, 64, 64, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 16, None)
+    st = lib.llmint8_matmul_int8(P(FAKE), 32, 64, 64, P(FAKE), P(FAKE), P(FAKE), P(FAKE), 16, None)
     assert st == _lib.EWORKSPACE
 
 
 def test_quantize_weight_argument_errors(lib):
     P = ctypes.c_void_p
-    assert lib.llmint8_quantize_weight(P(0), 64, 64, P(FAKE), P(FAKE), None, None) == _lib.EINVAL
-    assert lib.llmint8_quantize_weight(P(FAKE), 0, 64, P(FAKE), P(FAKE), None, None) == _lib.EINVAL
-    assert lib.llmint8_quantize_weight(P(FAKE), 65, 64, P(FAKE), P(FAKE), None, None) == _lib.EALIGN
-    assert lib.llmint8_quantize_weight(P(FAKE), 64, 64, P(FAKE + 4), P(FAKE), None, None) == _lib.EALIGN
+    assert lib.llmint8_quantize_weight(P(0), 64, 64, P(FAKE), P(FAKE), None) == _lib.EINVAL
+    assert lib.llmint8_quantize_weight(P(FAKE), 0, 64, P(FAKE), P(FAKE), None) == _lib.EINVAL
+    assert lib.llmint8_quantize_weight(P(FAKE), 65, 64, P(FAKE), P(FAKE), None) == _lib.EALIGN
+    assert lib.llmint8_quantize_weight(P(FAKE), 64, 64, P(FAKE + 4), P(FAKE), None) == _lib.EALIGN
 
 
 def test_noalloc_argument_errors(lib):
     P = ctypes.c_void_p
     # shapes whose workspace exceeds the static 8 MiB scratch are rejected on the host
-    assert lib.llmint8_matmul_noalloc(P(FAKE), 4096, 8192, 8192, 6.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+    assert lib.llmint8_matmul_noalloc(P(FAKE), 4096, 8192, 8192, 6.0, P(FAKE), P(FAKE), P(FAKE),
                                       P(FAKE), None) == _lib.EWORKSPACE
-    assert lib.llmint8_matmul_noalloc(P(FAKE), 0, 64, 64, 6.0, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+    assert lib.llmint8_matmul_noalloc(P(FAKE), 0, 64, 64, 6.0, P(FAKE), P(FAKE), P(FAKE),
                                       P(FAKE), None) == _lib.EINVAL
 
 
@@ -160,7 +160,7 @@ def test_matmul_host_argument_errors(lib):
     P = ctypes.c_void_p
     ws = lib.llmint8_workspace_bytes(4, 64, 64)
     call = lambda xh=FAKE, yh=FAKE, Y=FAKE, M=4, wsb=ws: lib.llmint8_matmul_host(
-        P(xh) if xh else None, P(FAKE), M, 64, 64, 6.0, P(FAKE), P(FAKE), None, P(FAKE), P(Y) if Y else None,
+        P(xh) if xh else None, P(FAKE), M, 64, 64, 6.0, P(FAKE), P(FAKE), P(FAKE), P(Y) if Y else None,
         P(yh) if yh else None, P(FAKE), wsb, None)
     assert call(xh=0) == _lib.EINVAL
     assert call(yh=0) == _lib.EINVAL
@@ -214,11 +214,11 @@ def test_kernels_per_call(lib):
         assert k(M, K, 4096, 6.0, 0) == 3, (M, K)
         assert k(M, K, 4096, inf, 0) == 2       # no outlier scan
     # prefill: scan + row quantization (which also gathers the outlier rows of W16
-    # when rows have at most 4096 columns) + GEMM
-    assert k(17, 4096, 4096, 6.0, 0) == 3
-    assert k(17, 4112, 4096, 6.0, 0) == 4       # separate gather of the outlier rows of W16
-    assert k(17, 4096, 4096, 6.0, 1) == 3       # the int32 result leaves out the fp16 slice
-    assert k(17, 4096, 4096, inf, 0) == 2
+    # when rows have at most 4096 columns) + widening of the codes + GEMM
+    assert k(17, 4096, 4096, 6.0, 0) == 4
+    assert k(17, 4112, 4096, 6.0, 0) == 5       # separate gather of the outlier rows of W16
+    assert k(17, 4096, 4096, 6.0, 1) == 4       # the int32 result leaves out the fp16 slice
+    assert k(17, 4096, 4096, inf, 0) == 3
     assert k(0, 64, 64, 6.0, 0) == -1
     assert k(1, 64, 64, math.nan, 0) == -1
 
@@ -227,7 +227,7 @@ def test_w8_argument_errors(lib):
     from bit_quantization_matmul_row_b300 import _lib
     P = ctypes.c_void_p
     ws = lib.llmint8_workspace_bytes(16, 64, 64)
-    args = lambda W16c, rmap, rows: (P(FAKE), 16, 64, 64, 6.0, P(FAKE), P(FAKE), P(FAKE), W16c, rmap, rows,
+    args = lambda W16c, rmap, rows: (P(FAKE), 16, 64, 64, 6.0, P(FAKE), P(FAKE), W16c, rmap, rows,
                                      P(FAKE), P(FAKE), ws, None)
     assert lib.llmint8_matmul_w8(*args(None, None, -1)) == _lib.EINVAL
     assert lib.llmint8_matmul_w8(*args(None, P(FAKE), 4)) == _lib.EINVAL   # rows kept, no W16c
@@ -240,8 +240,8 @@ def test_w8_argument_errors(lib):
 def test_bf16_argument_errors(lib):
     from bit_quantization_matmul_row_b300 import _lib
     P = ctypes.c_void_p
-    assert lib.llmint8_quantize_weight_bf16(P(0), 64, 64, P(FAKE), P(FAKE), None, None) == _lib.EINVAL
-    assert lib.llmint8_quantize_weight_bf16(P(FAKE), 65, 64, P(FAKE), P(FAKE), None, None) == _lib.EALIGN
+    assert lib.llmint8_quantize_weight_bf16(P(0), 64, 64, P(FAKE), P(FAKE), None) == _lib.EINVAL
+    assert lib.llmint8_quantize_weight_bf16(P(FAKE), 65, 64, P(FAKE), P(FAKE), None) == _lib.EALIGN
     ws = lib.llmint8_workspace_bytes(16, 64, 64)
-    assert lib.llmint8_matmul_bf16(P(FAKE), 16, 64, 64, 6.0, P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), P(FAKE), ws,
+    assert lib.llmint8_matmul_bf16(P(FAKE), 16, 64, 64, 6.0, P(FAKE), P(FAKE), None, P(FAKE), P(FAKE), ws,
                                    None) == _lib.EINVAL  # finite threshold without W16

@@ -37,11 +37,11 @@ def check_bf16(M, K, N, t, frac=0.01, seed=0):
     X, _ = synthetic.make_x(M, K, frac=frac, min_count=3 if frac else 0, seed=seed, fmt="bf16")
     W, _ = synthetic.make_w(K, N, seed=seed, fmt="bf16")
     Xd, Wd = _dev(X), _dev(W)
-    Wq, sw, Wq16 = api.llmint8_quantize_weight_bf16(Wd)
+    Wq, sw = api.llmint8_quantize_weight_bf16(Wd)
     ws = api.make_workspace(M, K, N, Xd.device)
-    Y = api.llmint8_matmul_bf16(Xd, t, Wq, sw, Wq16, Wd, workspace=ws)
+    Y = api.llmint8_matmul_bf16(Xd, t, Wq, sw, Wd, workspace=ws)
     inter = api.read_intermediates(ws, M, K, N)
-    C = api.llmint8_matmul_i32_bf16(Xd, t, Wq, sw, Wq16, workspace=api.make_workspace(M, K, N, Xd.device))
+    C = api.llmint8_matmul_i32_bf16(Xd, t, Wq, sw, workspace=api.make_workspace(M, K, N, Xd.device))
     torch.cuda.synchronize()
     assert api.llmint8_device_status(ws) == 0
     ref = oracle.llmint8_matmul(X, W, t, fmt="bf16")
@@ -89,8 +89,8 @@ def test_bf16_range_beyond_fp16():
     X[:, 7] = synthetic.to_bf16_bits(np.full(M, 1.0e6, np.float32))
     W, _ = synthetic.make_w(K, N, sigma=1e-6, seed=80, fmt="bf16")
     Xd, Wd = _dev(X), _dev(W)
-    Wq, sw, Wq16 = api.llmint8_quantize_weight_bf16(Wd)
-    Y = api.llmint8_matmul_bf16(Xd, 6.0, Wq, sw, Wq16, Wd)
+    Wq, sw = api.llmint8_quantize_weight_bf16(Wd)
+    Y = api.llmint8_matmul_bf16(Xd, 6.0, Wq, sw, Wd)
     torch.cuda.synchronize()
     ref = oracle.llmint8_matmul(X, W, 6.0, fmt="bf16")
     assert 7 in ref["outliers"]

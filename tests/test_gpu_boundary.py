@@ -90,7 +90,7 @@ def test_chain_with_state_derives_the_oracle_codes(M, K, N, frac):
     X, _ = synthetic.make_x(M, K, frac=frac, min_count=3, seed=M * 11 + K)
     W, _ = synthetic.make_w(K, N, seed=K + 7 * N)
     Wd = torch.from_numpy(W).cuda()
-    Wq, sw, _ = api.llmint8_quantize_weight(Wd, fp16_codes=False)
+    Wq, sw = api.llmint8_quantize_weight(Wd)
     ws = api.make_workspace(M, K, N)
     ws.fill_(0x5A)
     C = torch.empty((M, N), dtype=torch.int32, device="cuda")
@@ -115,7 +115,7 @@ def test_chain_rejects_a_state_of_another_shape():
     X, _ = synthetic.make_x(M, K, frac=0.0, min_count=0, seed=1)
     W, _ = synthetic.make_w(K, N, seed=2)
     Wd = torch.from_numpy(W).cuda()
-    Wq, sw, _ = api.llmint8_quantize_weight(Wd, fp16_codes=False)
+    Wq, sw = api.llmint8_quantize_weight(Wd)
     for hdr in ([M, 2 * K, 1], [M + 1, K, 1], [M, K, 0], [M, K, K // 16 + 1]):
         S = _state_from_oracle(X, 6.0)
         S[:12] = torch.from_numpy(np.array(hdr, np.int32).view(np.uint8)).cuda()
@@ -137,15 +137,15 @@ def test_matmul_host_equals_the_device_call(M, K, N):
     X, _ = synthetic.make_x(M, K, frac=0.001, min_count=4, seed=M + K)
     W, _ = synthetic.make_w(K, N, seed=N)
     Wd = torch.from_numpy(W).cuda()
-    Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd)
+    Wq, sw = api.llmint8_quantize_weight(Wd)
     Xh = torch.from_numpy(X).pin_memory()
     Xd = torch.empty((M, K), dtype=torch.float16, device="cuda")
     Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
     Yh = torch.empty((M, N), dtype=torch.float16).pin_memory()
     ws = api.make_workspace(M, K, N)
-    api.llmint8_matmul_host(Xh, Xd, 6.0, Wq, sw, Wq16, Wd, Y, Yh, ws)
+    api.llmint8_matmul_host(Xh, Xd, 6.0, Wq, sw, Wd, Y, Yh, ws)
     torch.cuda.synchronize()
-    Yref = api.llmint8_matmul(torch.from_numpy(X).cuda(), 6.0, Wq, sw, Wq16, Wd)
+    Yref = api.llmint8_matmul(torch.from_numpy(X).cuda(), 6.0, Wq, sw, Wd)
     torch.cuda.synchronize()
     assert torch.equal(Yh, Yref.cpu())
     ok, _ = y_close(Yh.numpy(), oracle.llmint8_matmul(X, W, 6.0)["Y"])

@@ -34,7 +34,7 @@ def _cuda():
 def _weights(K, N, seed):
     W, _ = synthetic.make_w(K, N, seed=seed)
     Wd = torch.from_numpy(W).cuda()
-    Wq, sw, _ = api.llmint8_quantize_weight(Wd, fp16_codes=False)
+    Wq, sw = api.llmint8_quantize_weight(Wd)
     return W, Wd, Wq, sw
 
 
@@ -127,7 +127,7 @@ def test_chained_calls_agree_with_llmint8_matmul(M):
         S_out = api.make_chain_state(M, N)
         Y = api.llmint8_matmul_chain(Xg, 6.0, S_in, Wq, sw, Wd, next_threshold=4.0, state_out=S_out)
         # the same layer through the workspace path, on the same X, with the threshold the state stands for
-        Y_std = api.llmint8_matmul(Xg, 6.0 if li == 0 else 4.0, Wq, sw, None, Wd)
+        Y_std = api.llmint8_matmul(Xg, 6.0 if li == 0 else 4.0, Wq, sw, Wd)
         torch.cuda.synchronize()
         ok, ratio = y_close(Y.cpu().numpy(), Y_std.cpu().numpy())
         assert ok, f"layer {li}: worst error/tolerance {ratio:.3g}"

@@ -197,12 +197,12 @@ def test_workspace_reused_by_consecutive_calls(M, K, N):
     W, _ = synthetic.make_w(K, N, seed=K + N)
     dev = torch.device("cuda")
     Wd = torch.from_numpy(W).to(dev)
-    Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd)
+    Wq, sw = api.llmint8_quantize_weight(Wd)
     ws = api.make_workspace(M, K, N, dev)
     Xs = [synthetic.make_x(M, K, frac=0.005 * (j + 1), min_count=2 + 3 * j, seed=500 + j)[0] for j in range(3)]
     Ys = []
     for X in Xs:
-        Ys.append(api.llmint8_matmul(torch.from_numpy(X).to(dev), 6.0, Wq, sw, Wq16, Wd, workspace=ws))
+        Ys.append(api.llmint8_matmul(torch.from_numpy(X).to(dev), 6.0, Wq, sw, Wd, workspace=ws))
     torch.cuda.synchronize()
     assert api.llmint8_device_status(ws) == 0
     wq = oracle.quantize_weight(W)

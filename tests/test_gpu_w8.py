@@ -32,17 +32,17 @@ def _run(M, K, N, keep, frac, seed):
     W, _ = synthetic.make_w(K, N, seed=seed)
     dev = torch.device("cuda")
     Xd, Wd = torch.from_numpy(X).to(dev), torch.from_numpy(W).to(dev)
-    Wq, sw, Wq16 = api.llmint8_quantize_weight(Wd)
+    Wq, sw = api.llmint8_quantize_weight(Wd)
     rows = _rows(keep, X, K, 6.0)
     W16c, row_map = api.llmint8_pack_w16_rows(Wd, torch.from_numpy(rows).to(dev))
     ws = api.make_workspace(M, K, N, dev)
-    Y = api.llmint8_matmul_w8(Xd, 6.0, Wq, sw, Wq16, W16c, row_map, workspace=ws)
+    Y = api.llmint8_matmul_w8(Xd, 6.0, Wq, sw, W16c, row_map, workspace=ws)
     torch.cuda.synchronize()
     assert api.llmint8_device_status(ws) == 0
     ref = oracle.llmint8_matmul(X, W, 6.0, w16_rows=rows)
     ok, ratio = y_close(Y.cpu().numpy(), ref["Y"])
     assert ok, ratio
-    return X, Xd, Wd, Wq, sw, Wq16, Y
+    return X, Xd, Wd, Wq, sw, Y
 
 
 @pytest.mark.parametrize("M,K,N,keep,frac", [
@@ -68,8 +68,8 @@ def test_w8_persistent_gemv(M, keep, frac):
 
 @pytest.mark.parametrize("M", [3, 200])
 def test_w8_with_every_row_kept_is_llmint8_matmul(M):
-    X, Xd, Wd, Wq, sw, Wq16, Y = _run(M, 1088, 272, "all", 0.02, seed=400 + M)
-    Yf = api.llmint8_matmul(Xd, 6.0, Wq, sw, Wq16, Wd)
+    X, Xd, Wd, Wq, sw, Y = _run(M, 1088, 272, "all", 0.02, seed=400 + M)
+    Yf = api.llmint8_matmul(Xd, 6.0, Wq, sw, Wd)
     torch.cuda.synchronize()
     assert torch.equal(Y.view(torch.int16), Yf.view(torch.int16))
 
