@@ -26,6 +26,7 @@ EXPORTS = (
     "llmint8_matmul_bf16",
     "llmint8_matmul_i32_bf16",
     "llmint8_matmul_i32",
+    "llmint8_gemm_i32",
     "llmint8_xpass",
     "llmint8_gemm",
     "llmint8_chain_state_bytes",
@@ -73,6 +74,7 @@ def load() -> ctypes.CDLL:
         lib.llmint8_matmul_bf16.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_i32_bf16.argtypes = [P, I, I, I, F, P, P, P, P, Z, P]
         lib.llmint8_matmul_i32.argtypes = [P, I, I, I, F, P, P, P, P, Z, P]
+        lib.llmint8_gemm_i32.argtypes = [P, P, I, I, I, P, P, Z, P]
         lib.llmint8_xpass.argtypes = [P, I, I, I, F, P, Z, P]
         lib.llmint8_gemm.argtypes = [P, I, I, I, F, P, P, P, P, P, Z, P]
         lib.llmint8_matmul_noalloc.argtypes = [P, I, I, I, F, P, P, P, P, P]
@@ -89,6 +91,7 @@ def load() -> ctypes.CDLL:
         lib.llmint8_device_status.argtypes = [P, P]
         lib.llmint8_selftest_timeout.argtypes = [P, I, P]
         for f in ("llmint8_quantize_weight", "llmint8_matmul", "llmint8_matmul_host", "llmint8_matmul_int8", "llmint8_matmul_i32",
+                  "llmint8_gemm_i32",
                   "llmint8_matmul_w8", "llmint8_pack_w16_rows", "llmint8_quantize_weight_bf16",
                   "llmint8_matmul_bf16", "llmint8_matmul_i32_bf16",
                   "llmint8_xpass", "llmint8_gemm", "llmint8_matmul_noalloc", "llmint8_chain_state_layout",

@@ -338,6 +338,23 @@ def llmint8_xpass(X, threshold, N, workspace, stream=None):
     _check(st, "llmint8_xpass")
 
 
+def llmint8_gemm_i32(Xq, Wq, C=None, workspace=None, stream=None):
+    """A3 on caller codes: Xq int8 [M, K], Wq int8 [N, K] -> exact C int32 [M, N]."""
+    M, K = Xq.shape
+    N = Wq.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.int32, device=Xq.device)
+    if workspace is None:
+        workspace = make_workspace(M, K, N, Xq.device)
+    _need(Xq, torch.int8, (M, K), "Xq")
+    _need(Wq, torch.int8, (N, K), "Wq")
+    _need(C, torch.int32, (M, N), "C")
+    st = _lib.load().llmint8_gemm_i32(_ptr(Xq), _ptr(Wq), M, K, N, _ptr(C), _ptr(workspace), workspace.numel(),
+                                      _stream(stream, Xq))
+    _check(st, "llmint8_gemm_i32")
+    return C
+
+
 def llmint8_gemm(X, threshold, Wq, colScaleW, W16, Y, workspace, stream=None):
     """A3..A5 from a workspace filled by llmint8_xpass (second half of llmint8_matmul)."""
     M, K, N = _shapes(X, Wq)

@@ -362,14 +362,16 @@ template <typename T>
 llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
                            const float* colScaleW, const void* W16, void* out, bool write_i32,
                            void* workspace, const Layout& L, DeviceInfo* dev, cudaStream_t s,
-                           bool w16o_ready = false, const W16Src& src = W16Src()) {
+                           bool w16o_ready = false, const W16Src& src = W16Src(),
+                           const int8_t* codes8 = nullptr) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
     const WsView w(workspace, L);
     llmint8_status st;
 
     if (L.decode) {
         GemvArgs ga;
-        ga.codes = reinterpret_cast<const int8_t*>(w.codes);
+        // the X pass's int8 codes, or the caller's (llmint8_gemm_i32)
+        ga.codes = codes8 ? codes8 : reinterpret_cast<const int8_t*>(w.codes);
         ga.Wq = Wq;
         ga.col_scale = colScaleW;
         ga.row_scale = w.row_scale;
@@ -768,6 +770,29 @@ llmint8_status llmint8_matmul_i32(const void* X, int M, int K, int N, float thre
                                   size_t workspace_bytes, void* stream) {
     return matmul_impl(X, M, K, N, threshold, Wq, colScaleW, nullptr, C, true, workspace, workspace_bytes,
                        stream);
+}
+
+llmint8_status llmint8_gemm_i32(const int8_t* Xq, const int8_t* Wq, int M, int K, int N, int32_t* C,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+    if (!Xq || !Wq || !C || !sizes_ok(M, K, N)) return LLMINT8_EINVAL;
+    if ((K % 16) || (N % 16)) return LLMINT8_EALIGN;
+    if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(C) || !aligned16(workspace)) return LLMINT8_EALIGN;
+    const Layout L = make_layout(M, K, N);
+    if (!workspace || workspace_bytes < L.total) return LLMINT8_EWORKSPACE;
+    DeviceInfo* dev = nullptr;
+    llmint8_status st = current_device(&dev);
+    if (st != LLMINT8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (L.decode)  // the GEMV reads the caller's codes where the X pass would leave its own
+        return gemm_launch<__half>(nullptr, M, K, N, INFINITY, Wq, nullptr, nullptr, C, true, workspace, L, dev, s,
+                                   false, W16Src(), Xq);
+    // the tensor-core GEMM reads the codes as exact fp16 integers from the workspace
+    const WsView w(workspace, L);
+    const size_t n16 = (size_t)M * K / 16;
+    const size_t want = (n16 + 256 * kWidenUnroll - 1) / (256 * kWidenUnroll), cap = (size_t)dev->sms * 8;
+    st = launch(k_widen_codes, dim3((unsigned)(want < cap ? want : cap)), dim3(256), 0, s, true, Xq, w.codes, n16);
+    if (st != LLMINT8_OK) return st;
+    return gemm_launch<__half>(nullptr, M, K, N, INFINITY, Wq, nullptr, nullptr, C, true, workspace, L, dev, s);
 }
 
 llmint8_status llmint8_xpass(const void* X, int M, int K, int N, float threshold, void* workspace,

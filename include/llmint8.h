@@ -104,8 +104,8 @@ size_t llmint8_workspace_bytes(int M, int K, int N);
  * Source: paper walkthrough, sections 2.1-2.3; pitfalls guide, sections 3.1-3.3.
  */
 llmint8_status llmint8_matmul(const void *X, int M, int K, int N, float threshold,
-                              const int8_t *Wq, const float *colScaleW, const void *W16, void *Y,
-                              void *workspace, size_t workspace_bytes,
+                              const int8_t *Wq, const float *colScaleW,
+                              const void *W16, void *Y, void *workspace, size_t workspace_bytes,
                               void *stream);
 
 /*
@@ -126,10 +126,9 @@ llmint8_status llmint8_matmul(const void *X, int M, int K, int N, float threshol
  * Errors as llmint8_matmul (all checked before the first copy is enqueued);
  * EINVAL also for a NULL X_host, Y_host or Y; ECUDA if a copy cannot be enqueued.
  */
-llmint8_status llmint8_matmul_host(const void *X_host, void *X, int M, int K, int N,
-float threshold,
-                                   const int8_t *Wq, const float *colScaleW, const void *W16,
-                                   void *Y, void *Y_host, void *workspace,
+llmint8_status llmint8_matmul_host(const void *X_host, void *X, int M, int K, int N, float threshold,
+                                   const int8_t *Wq, const float *colScaleW,
+                                   const void *W16, void *Y, void *Y_host, void *workspace,
                                    size_t workspace_bytes, void *stream);
 
 /*
@@ -140,16 +139,15 @@ float threshold,
  * is rounded to bf16 (nearest even).
  * llmint8_matmul_i32_bf16 writes the int32 accumulator C, as llmint8_matmul_i32.
  */
-llmint8_status llmint8_quantize_weight_bf16(const void *W, int K, int N, int8_t *Wq,
-float *colScaleW,
+llmint8_status llmint8_quantize_weight_bf16(const void *W, int K, int N, int8_t *Wq, float *colScaleW,
                                             void *stream);
 llmint8_status llmint8_matmul_bf16(const void *X, int M, int K, int N, float threshold,
-                                   const int8_t *Wq, const float *colScaleW, const void *W16,
-                                   void *Y, void *workspace, size_t workspace_bytes,
+                                   const int8_t *Wq, const float *colScaleW,
+                                   const void *W16, void *Y, void *workspace, size_t workspace_bytes,
                                    void *stream);
 llmint8_status llmint8_matmul_i32_bf16(const void *X, int M, int K, int N, float threshold,
-                                       const int8_t *Wq, const float *colScaleW, int32_t *C,
-                                       void *workspace, size_t workspace_bytes, void *stream);
+                                       const int8_t *Wq, const float *colScaleW,
+                                       int32_t *C, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * llmint8_matmul without a full fp16 copy of W (int8 weight storage only).  The
@@ -176,8 +174,8 @@ llmint8_status llmint8_matmul_i32_bf16(const void *X, int M, int K, int N, float
  * page, section 2.2 (one scale per output column).
  */
 llmint8_status llmint8_matmul_w8(const void *X, int M, int K, int N, float threshold,
-                                 const int8_t *Wq, const float *colScaleW, const void *W16c,
-                                 const int32_t *row_map, int w16_rows, void *Y,
+                                 const int8_t *Wq, const float *colScaleW,
+                                 const void *W16c, const int32_t *row_map, int w16_rows, void *Y,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -198,8 +196,7 @@ llmint8_status llmint8_matmul_w8(const void *X, int M, int K, int N, float thres
  * or W16 or W16c is not 16-byte aligned; ECUDA if a launch fails.  Asynchronous
  * on `stream`.
  */
-llmint8_status llmint8_pack_w16_rows(const void *W16, int K, int N, const int32_t *rows,
-int w16_rows,
+llmint8_status llmint8_pack_w16_rows(const void *W16, int K, int N, const int32_t *rows, int w16_rows,
                                      void *W16c, int32_t *row_map, void *stream);
 
 /*
@@ -244,8 +241,7 @@ llmint8_status llmint8_gemm(const void *X, int M, int K, int N, float threshold,
  * Same rules as llmint8_matmul for X, M, K and threshold; EINVAL for a NULL Xq
  * or rowScaleX, EALIGN for one that is not 16-byte aligned.  Asynchronous.
  */
-llmint8_status llmint8_quantize_x(const void *X, int M, int K, float threshold, int8_t *Xq,
-float *rowScaleX,
+llmint8_status llmint8_quantize_x(const void *X, int M, int K, float threshold, int8_t *Xq, float *rowScaleX,
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -259,8 +255,7 @@ float *rowScaleX,
  * stored count outside [0, K] (a workspace no X pass of this K has filled);
  * ECUDA if synchronization or a copy fails.
  */
-llmint8_status llmint8_read_outliers(const void *workspace, int K, int *count, int32_t *idx_host,
-int capacity,
+llmint8_status llmint8_read_outliers(const void *workspace, int K, int *count, int32_t *idx_host, int capacity,
                                      void *stream);
 
 /*
@@ -309,10 +304,8 @@ int capacity,
  * one.  Asynchronous on `stream`.
  */
 size_t llmint8_chain_state_bytes(int M, int N);
-llmint8_status llmint8_chain_state_layout(int M, int N, size_t *offsets /* [3]: flags, parts,
-total */);
-llmint8_status llmint8_matmul_chain(const void *X, int M, int K, int N, float threshold,
-const void *state_in,
+llmint8_status llmint8_chain_state_layout(int M, int N, size_t *offsets /* [3]: flags, parts, total */);
+llmint8_status llmint8_matmul_chain(const void *X, int M, int K, int N, float threshold, const void *state_in,
                                     size_t state_in_bytes, const int8_t *Wq, const float *colScaleW,
                                     const void *W16, void *Y, float next_threshold, void *state_out,
                                     size_t state_out_bytes, void *workspace, size_t workspace_bytes,
@@ -323,12 +316,9 @@ const void *state_in,
  * kernel derives from a state are then checkable bit for bit).  Same arguments
  * and errors, plus C (16-byte aligned, not NULL).
  */
-llmint8_status llmint8_matmul_chain_i32(const void *X, int M, int K, int N, float threshold,
-const void *state_in,
-                                        size_t state_in_bytes, const int8_t *Wq,
-                                        const float *colScaleW,
-                                        const void *W16, void *Y, float next_threshold,
-                                        void *state_out,
+llmint8_status llmint8_matmul_chain_i32(const void *X, int M, int K, int N, float threshold, const void *state_in,
+                                        size_t state_in_bytes, const int8_t *Wq, const float *colScaleW,
+                                        const void *W16, void *Y, float next_threshold, void *state_out,
                                         size_t state_out_bytes, int32_t *C, void *workspace,
                                         size_t workspace_bytes, void *stream);
 
@@ -355,8 +345,8 @@ const void *state_in,
  *     llmint8_device_status.
  */
 llmint8_status llmint8_matmul_noalloc(const void *X, int M, int K, int N, float threshold,
-                                      const int8_t *Wq, const float *colScaleW, const void *W16,
-                                      void *Y, void *stream);
+                                      const int8_t *Wq, const float *colScaleW,
+                                      const void *W16, void *Y, void *stream);
 
 /* ----------------------------------------------------------------------------
  * Introspection (tests and diagnostics; not on the hot path)
@@ -371,9 +361,33 @@ llmint8_status llmint8_matmul_noalloc(const void *X, int M, int K, int N, float 
  * zeroed, and W16 is not needed.
  */
 llmint8_status llmint8_matmul_i32(const void *X, int M, int K, int N, float threshold,
-                                  const int8_t *Wq, const float *colScaleW, int32_t *C,
-                                  void *workspace, size_t workspace_bytes,
+                                  const int8_t *Wq, const float *colScaleW,
+                                  int32_t *C, void *workspace, size_t workspace_bytes,
                                   void *stream);
+
+/*
+ * A3 alone on codes the caller chooses: C = Xq . Wq^T, exact int32, through the
+ * same kernels the matmul uses (the int8 GEMV for M <= LLMINT8_DECODE_MAX_M;
+ * above, the codes of Xq and Wq widened to exact fp16 integers and the
+ * tensor-core GEMM with its 1024-long fp32 chunks drained into int32).  The
+ * int8 x int8 -> int32 product the pages rescale afterwards ("Lightning Fabric
+ * 8-bit" page, section 2.2; paper walkthrough, section 2.3).
+ *
+ *   Xq         in   int8 [M, K] row-major, any values in [-127, 127] (-128 is
+ *                   accepted and multiplied as -128, but |C| < 2^31 is then the
+ *                   caller's concern)
+ *   Wq         in   int8 [N, K] row-major (the layout llmint8_quantize_weight
+ *                   writes), values as Xq
+ *   C          out  int32 [M, N] row-major, C[i,n] = sum_k Xq[i,k] * Wq[n,k]
+ *   workspace  at least llmint8_workspace_bytes(M, K, N) bytes (its code and
+ *              weight-code scratch are overwritten)
+ *
+ * EINVAL for NULL Xq, Wq or C or sizes as llmint8_matmul; EALIGN for K or N not
+ * a multiple of 16 or an unaligned pointer; EWORKSPACE as llmint8_matmul.
+ * Asynchronous on `stream`.
+ */
+llmint8_status llmint8_gemm_i32(const int8_t *Xq, const int8_t *Wq, int M, int K, int N, int32_t *C,
+                                void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Number of kernels one llmint8_matmul (write_i32 = 0) or llmint8_matmul_i32

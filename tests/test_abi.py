@@ -245,3 +245,22 @@ def test_bf16_argument_errors(lib):
     ws = lib.llmint8_workspace_bytes(16, 64, 64)
     assert lib.llmint8_matmul_bf16(P(FAKE), 16, 64, 64, 6.0, P(FAKE), P(FAKE), None, P(FAKE), P(FAKE), ws,
                                    None) == _lib.EINVAL  # finite threshold without W16
+
+
+def test_gemm_i32_argument_errors(lib):
+    P = ctypes.c_void_p
+    ws = lib.llmint8_workspace_bytes(32, 64, 64)
+    call = lambda xq=FAKE, wq=FAKE, C=FAKE, M=32, K=64, N=64, w=FAKE, wsb=ws: lib.llmint8_gemm_i32(
+        P(xq) if xq else None, P(wq) if wq else None, M, K, N, P(C) if C else None, P(w) if w else None, wsb, None)
+    assert call(xq=0) == _lib.EINVAL
+    assert call(wq=0) == _lib.EINVAL
+    assert call(C=0) == _lib.EINVAL
+    assert call(M=0) == _lib.EINVAL
+    assert call(K=40) == _lib.EALIGN
+    assert call(N=24) == _lib.EALIGN
+    assert call(xq=FAKE + 4) == _lib.EALIGN
+    assert call(w=0) == _lib.EWORKSPACE
+    assert call(wsb=ws - 16) == _lib.EWORKSPACE
+    # the workspace the matmul of the same shape needs is enough (decode and prefill)
+    for M in (1, 16, 17, 300):
+        assert lib.llmint8_workspace_bytes(M, 1088, 400) > 0
