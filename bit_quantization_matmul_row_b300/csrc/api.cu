@@ -34,6 +34,7 @@ struct DeviceInfo {
     bool gemv_attr_set[2] = {false, false};
     bool rowq_cluster_attr_set[2] = {false, false};
     bool chain_attr_set = false;
+    bool widen_attr_set = false;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -357,6 +358,24 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
     }
 }
 
+// k_widen_codes over nbytes int8 codes (-> exact fp16 integers at dst).
+llmint8_status widen_launch(const int8_t* src, __half* dst, size_t nbytes, bool src_constant, WsHeader* err,
+                            DeviceInfo* dev, cudaStream_t s, bool pdl) {
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!dev->widen_attr_set) {
+            if (cudaFuncSetAttribute(k_widen_codes, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWidenSmem) !=
+                cudaSuccess)
+                return LLMINT8_ECUDA;
+            dev->widen_attr_set = true;
+        }
+    }
+    const size_t nchunks = (nbytes + kWidenChunk - 1) / kWidenChunk;
+    const unsigned grid = (unsigned)(nchunks < (size_t)dev->sms ? nchunks : (size_t)dev->sms);
+    return launch(k_widen_codes, dim3(grid), dim3(kWidenThreads), kWidenSmem, s, pdl, src, dst, nbytes,
+                  src_constant ? 1 : 0, err, kDefaultSpinLimit);
+}
+
 // A3 + A4 + A5 from the workspace an xpass_launch of the same problem filled.
 template <typename T>
 llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, const int8_t* Wq,
@@ -439,13 +458,7 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         if (st != LLMINT8_OK) return st;
     }
     // A3 operand: the int8 codes widened to exact fp16 integers in the scratch
-    {
-        const size_t n16 = (size_t)N * K / 16;
-        const size_t want = (n16 + 256 * kWidenUnroll - 1) / (256 * kWidenUnroll);
-        const size_t cap = (size_t)dev->sms * 8;
-        st = launch(k_widen_codes, dim3((unsigned)(want < cap ? want : cap)), dim3(256), 0, s, true, Wq, w.wq16, n16);
-        if (st != LLMINT8_OK) return st;
-    }
+    if ((st = widen_launch(Wq, w.wq16, (size_t)N * K, true, w.hdr, dev, s, true)) != LLMINT8_OK) return st;
     if ((st = get_encoder()) != LLMINT8_OK) return st;
     // CTA pairs (256 x 256 tiles, each CTA loading 128 columns of B) once M
     // spans two 128-row tiles; 256 x 128 pair tiles when the wide ones would
@@ -788,10 +801,7 @@ llmint8_status llmint8_gemm_i32(const int8_t* Xq, const int8_t* Wq, int M, int K
                                    false, W16Src(), Xq);
     // the tensor-core GEMM reads the codes as exact fp16 integers from the workspace
     const WsView w(workspace, L);
-    const size_t n16 = (size_t)M * K / 16;
-    const size_t want = (n16 + 256 * kWidenUnroll - 1) / (256 * kWidenUnroll), cap = (size_t)dev->sms * 8;
-    st = launch(k_widen_codes, dim3((unsigned)(want < cap ? want : cap)), dim3(256), 0, s, true, Xq, w.codes, n16);
-    if (st != LLMINT8_OK) return st;
+    if ((st = widen_launch(Xq, w.codes, (size_t)M * K, false, w.hdr, dev, s, true)) != LLMINT8_OK) return st;
     return gemm_launch<__half>(nullptr, M, K, N, INFINITY, Wq, nullptr, nullptr, C, true, workspace, L, dev, s);
 }
 

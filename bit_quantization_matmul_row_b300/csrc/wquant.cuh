@@ -87,44 +87,99 @@ __global__ void __launch_bounds__(256) k_quantize_weight_tile(const __half* __re
     }
 }
 
-// Prefill operand of A3: the int8 codes Wq [N, K] as exact fp16 integers in a
-// per-call scratch of the same layout, which the tensor-core GEMM loads by TMA
-// (sm_103a has no int8 tcgen05 MMA; kind::f16 on exact integer codes stands in).
-// Each thread widens kWidenUnroll 16-code chunks per step (all loads issued
-// before the stores, grid-strided so that a warp touches 512 contiguous bytes).
-// The scratch is in the workspace, which the previous call's GEMM may still be
-// reading: the stores wait for the predecessor (programmatic dependent launch).
-constexpr int kWidenUnroll = 4;
-__global__ void __launch_bounds__(256, 8) k_widen_codes(const int8_t* __restrict__ Wq, __half* __restrict__ out,
-                                                     size_t n16) {
+// Prefill operand of A3: int8 codes as exact fp16 integers in a per-call
+// scratch of the same layout, which the tensor-core GEMM loads by TMA (sm_103a
+// has no int8 tcgen05 MMA; kind::f16 on exact integer codes stands in).  Used
+// for the weight codes Wq [N, K] and, by llmint8_gemm_i32, for caller codes of X.
+//
+// A bandwidth pass that keeps the load/store path of the SMs out of the way:
+// bulk copies (TMA engine) bring 32 KB slices of the codes into a ring of
+// kWidenIn shared-memory buffers, the CTA widens a slice into one of
+// kWidenOut output buffers (shared memory only), and a bulk store writes it
+// back.  One CTA per SM, grid-strided over slices.  The codes may be read
+// before the predecessor finishes only when they are constant (weights); the
+// scratch is written only after it (the previous call's GEMM may still read
+// it).  Waits are bounded: a timeout records the error word and the CTA stops
+// after letting its copies in flight finish.
+constexpr uint32_t kWidenChunk = 32768;  // int8 bytes per slice (one fence and barrier pair each)
+constexpr int kWidenIn = 3, kWidenOut = 2, kWidenThreads = 256;
+constexpr size_t kWidenSmem = 1024 + (size_t)kWidenIn * kWidenChunk + (size_t)kWidenOut * 2 * kWidenChunk + 256;
+static_assert(kWidenSmem <= 232448, "one CTA per SM within the opt-in shared memory limit");
+
+__global__ void __launch_bounds__(kWidenThreads, 1)
+    k_widen_codes(const int8_t* __restrict__ src, __half* __restrict__ dst, size_t nbytes, int src_constant,
+                  WsHeader* err, uint32_t spin_limit) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* in = sm;                                                // [kWidenIn][kWidenChunk]
+    uint8_t* out = sm + (size_t)kWidenIn * kWidenChunk;              // [kWidenOut][2 * kWidenChunk]
+    uint64_t* full = reinterpret_cast<uint64_t*>(out + (size_t)kWidenOut * 2 * kWidenChunk);  // [kWidenIn]
+    __shared__ uint32_t s_ok;
+    const int tid = threadIdx.x;
+    const size_t nchunks = (nbytes + kWidenChunk - 1) / kWidenChunk;
+    auto chunk_of = [&](size_t j) { return (size_t)blockIdx.x + j * gridDim.x; };
+    auto bytes_of = [&](size_t c) {
+        const size_t rest = nbytes - c * kWidenChunk;
+        return (uint32_t)(rest < kWidenChunk ? rest : kWidenChunk);
+    };
+    auto issue = [&](size_t j) {  // thread 0: slice j of this CTA into ring slot j % kWidenIn
+        const size_t c = chunk_of(j);
+        if (c >= nchunks) return;
+        uint64_t* bar = &full[j % kWidenIn];
+        mbar_arrive_expect_tx(bar, bytes_of(c));
+        bulk_load_1d(in + (j % kWidenIn) * kWidenChunk, src + c * kWidenChunk, bytes_of(c), bar);
+    };
+    if (tid == 0) {
+        for (int i = 0; i < kWidenIn; ++i) mbar_init(&full[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
     pdl_trigger();
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
-    bool waited = false;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += kWidenUnroll * stride) {
-        uint4 v[kWidenUnroll];
-#pragma unroll
-        for (int u = 0; u < kWidenUnroll; ++u) {
-            const size_t c = i + u * stride;
-            v[u] = c < n16 ? ldg_nc_v4(Wq + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+    if (!src_constant) pdl_wait();
+    if (tid == 0)
+        for (int i = 0; i < kWidenIn; ++i) issue(i);
+    pdl_wait();
+    size_t j = 0;
+    for (; chunk_of(j) < nchunks; ++j) {
+        const size_t c = chunk_of(j);
+        const int si = (int)(j % kWidenIn), so = (int)(j % kWidenOut);
+        if (tid == 0) {
+            // the output slot's previous bulk store has finished reading it
+            if (j >= (size_t)kWidenOut) bulk_wait_read<kWidenOut - 1>();
+            s_ok = mbar_wait_bounded(&full[si], (uint32_t)(j / kWidenIn) & 1u, spin_limit, nullptr) ? 1u : 0u;
         }
-        if (!waited) {
-            pdl_wait();
-            waited = true;
+        __syncthreads();
+        if (!s_ok) break;
+        const uint32_t nb = bytes_of(c);
+        const uint8_t* a = in + (size_t)si * kWidenChunk;
+        uint8_t* o = out + (size_t)so * 2 * kWidenChunk;
+#pragma unroll 4
+        for (uint32_t p = tid * 16; p < nb; p += kWidenThreads * 16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(a + p);
+            uint32_t h[8];
+            s8x4_to_half2x2(v.x, h[0], h[1]);
+            s8x4_to_half2x2(v.y, h[2], h[3]);
+            s8x4_to_half2x2(v.z, h[4], h[5]);
+            s8x4_to_half2x2(v.w, h[6], h[7]);
+            *reinterpret_cast<uint4*>(o + 2 * p) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(o + 2 * p + 16) = make_uint4(h[4], h[5], h[6], h[7]);
         }
-#pragma unroll
-        for (int u = 0; u < kWidenUnroll; ++u) {
-            const size_t c = i + u * stride;
-            if (c < n16) {
-                uint32_t h[8];
-                s8x4_to_half2x2(v[u].x, h[0], h[1]);
-                s8x4_to_half2x2(v[u].y, h[2], h[3]);
-                s8x4_to_half2x2(v[u].z, h[4], h[5]);
-                s8x4_to_half2x2(v[u].w, h[6], h[7]);
-                uint4* o = reinterpret_cast<uint4*>(out + c * 16);
-                o[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                o[1] = make_uint4(h[4], h[5], h[6], h[7]);
-            }
+        fence_proxy_async_smem();  // the bulk store reads these writes through the async proxy
+        __syncthreads();
+        if (tid == 0) {
+            bulk_store_1d(dst + c * kWidenChunk, o, 2 * nb);
+            bulk_commit();
+            issue(j + kWidenIn);  // the input slot is free again (all threads passed the barrier)
         }
+    }
+    if (tid == 0) {
+        if (!s_ok) {
+            record_error(err, kStatusTimeout, 30);
+            // let the loads already issued land before shared memory goes away
+            for (size_t k = j; k < j + kWidenIn && chunk_of(k) < nchunks; ++k)
+                mbar_wait_bounded(&full[k % kWidenIn], (uint32_t)(k / kWidenIn) & 1u, 1u << 20, nullptr);
+        }
+        bulk_wait_all();
     }
 }
 
