@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -258,9 +259,13 @@ struct WsView {
 
 // Prefill rows of at most 4096 columns run k_row_quant_warp, which can also
 // write the gathered outlier rows of W16 for the GEMM (no separate gather).
-bool rowq_gathers_w16(bool decode, int K, float threshold, bool write_i32, const void* W16) {
+// Only while its M/8 CTAs are enough for the N/16 column groups (at most 8
+// groups each): at M = 32, N = 11008 the 4 CTAs took 147 us for 688 groups,
+// where the separate gather kernel runs N/64 CTAs.
+bool rowq_gathers_w16(bool decode, int M, int K, int N, float threshold, bool write_i32, const void* W16) {
     const bool use_outliers = !(std::isinf(threshold) && threshold > 0);
-    return !decode && K <= 4096 && use_outliers && !write_i32 && W16 != nullptr;
+    const bool enough_ctas = (size_t)((M + kRowsPerCta - 1) / kRowsPerCta) * 8 >= (size_t)(N / kGatherCols);
+    return !decode && K <= 4096 && enough_ctas && use_outliers && !write_i32 && W16 != nullptr;
 }
 
 // Caller-owned destinations of A2 (llmint8_quantize_x): int8 codes [M, K] and
@@ -356,6 +361,27 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
         case 8: return launch(k_row_quant<8, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
         default: return launch(k_row_quant<0, T>, dim3(M), dim3(kRowThreads), 0, s, pdl, ra);
     }
+}
+
+// Tile shape and grid of the prefill GEMM (persistent over ctas_or_clusters).
+struct GemmPlan {
+    bool pair;
+    int bn, ctas_or_clusters;
+};
+
+GemmPlan gemm_plan(int M, int N, int K, int sms) {
+    GemmPlan g;
+    g.pair = M > kBM && sms >= 2;
+    const int tiles_m = g.pair ? (M + 2 * kBM - 1) / (2 * kBM) : (M + kBM - 1) / kBM;
+    const int slots = g.pair ? sms / 2 : sms;
+    if (g.pair)
+        g.bn = tiles_m * ((N + kBN - 1) / kBN) * 10 < 6 * slots ? 128 : kBN;
+    else
+        g.bn = tiles_m * ((N + kBN - 1) / kBN) * 2 <= slots ? 128 : kBN;
+    const int tiles = tiles_m * ((N + g.bn - 1) / g.bn);
+    g.ctas_or_clusters = tiles < slots ? tiles : slots;
+    (void)K;
+    return g;
 }
 
 // k_widen_codes over nbytes int8 codes (-> exact fp16 integers at dst).
@@ -457,17 +483,16 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
                     (const int32_t*)w.idx, w.w16o, L.kp, w8);
         if (st != LLMINT8_OK) return st;
     }
+    // Tiling.  CTA pairs (256 x 256 tiles, each CTA loading 128 columns of B)
+    // once M spans two 128-row tiles; 256 x 128 pair tiles when the wide ones
+    // would give fewer clusters than 60 % of the cluster slots (medium M); one
+    // CTA per 128 x 256 tile below, or 128 x 128 when that still leaves half the
+    // SMs idle.
+    const GemmPlan g = gemm_plan(M, N, K, dev->sms);
+    const int b_rows = g.pair ? g.bn / 2 : g.bn;
     // A3 operand: the int8 codes widened to exact fp16 integers in the scratch
     if ((st = widen_launch(Wq, w.wq16, (size_t)N * K, true, w.hdr, dev, s, true)) != LLMINT8_OK) return st;
     if ((st = get_encoder()) != LLMINT8_OK) return st;
-    // CTA pairs (256 x 256 tiles, each CTA loading 128 columns of B) once M
-    // spans two 128-row tiles; 256 x 128 pair tiles when the wide ones would
-    // give fewer clusters than 60 % of the cluster slots (medium M)
-    const bool pair = M > kBM && dev->sms >= 2;
-    const int tiles_m2 = (M + 2 * kBM - 1) / (2 * kBM);
-    const bool narrow = pair && tiles_m2 * ((N + kBN - 1) / kBN) * 10 < 6 * (dev->sms / 2);
-    const int bn = narrow ? 128 : kBN;
-    const int b_rows = pair ? bn / 2 : bn;
     CUtensorMap tm_a, tm_b, tm_xo, tm_wo;
     if ((st = encode_fp16_2d(&tm_a, w.codes, M, K, K, kBM)) != LLMINT8_OK) return st;
     if ((st = encode_fp16_2d(&tm_b, w.wq16, N, K, K, b_rows)) != LLMINT8_OK) return st;
@@ -476,18 +501,15 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!dev->gemm_attr_set[Fmt<T>::kBF16]) {
-            if (cudaFuncSetAttribute(k_gemm_tc<false, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kGemmSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(k_gemm_tc<true, false, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kGemmSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(k_gemm_tc<false, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kGemmSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(k_gemm_tc<true, true, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kGemmSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(k_gemm_tc<false, true, T, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kGemmSmem) != cudaSuccess ||
-                cudaFuncSetAttribute(k_gemm_tc<true, true, T, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kGemmSmem) != cudaSuccess)
+            const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+            if (cudaFuncSetAttribute(k_gemm_tc<false, false, T, 256>, attr, (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<true, false, T, 256>, attr, (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<false, false, T, 128>, attr, (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<true, false, T, 128>, attr, (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<false, true, T, 256>, attr, (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<true, true, T, 256>, attr, (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<false, true, T, 128>, attr, (int)kGemmSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(k_gemm_tc<true, true, T, 128>, attr, (int)kGemmSmem) != cudaSuccess)
                 return LLMINT8_ECUDA;
             dev->gemm_attr_set[Fmt<T>::kBF16] = true;
         }
@@ -504,30 +526,29 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
     // the int32 accumulator leaves the outlier slice out (it is not part of C)
     ga.use_outliers = (use_outliers && !write_i32) ? 1 : 0;
     ga.spin_limit = kDefaultSpinLimit;
-    if (pair) {
-        const int units = tiles_m2 * ((N + bn - 1) / bn);
-        const int clusters = units < dev->sms / 2 ? units : dev->sms / 2;
-        const dim3 grid(2 * clusters);
-        if (narrow) {
-            if (write_i32)
-                return launch_cluster(k_gemm_tc<true, true, T, 128>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u,
-                                      tm_a, tm_b, tm_xo, tm_wo, ga);
-            return launch_cluster(k_gemm_tc<false, true, T, 128>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u,
-                                  tm_a, tm_b, tm_xo, tm_wo, ga);
-        }
-        if (write_i32)
-            return launch_cluster(k_gemm_tc<true, true, T>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u, tm_a, tm_b,
-                                  tm_xo, tm_wo, ga);
-        return launch_cluster(k_gemm_tc<false, true, T>, grid, dim3(kGemmThreads), kGemmSmem, s, true, 2u, tm_a, tm_b,
-                              tm_xo, tm_wo, ga);
+    const dim3 block(kGemmThreads);
+    if (g.pair) {
+        const dim3 grid(2 * g.ctas_or_clusters);
+        if (g.bn == 128)
+            return write_i32 ? launch_cluster(k_gemm_tc<true, true, T, 128>, grid, block, kGemmSmem, s, true, 2u, tm_a,
+                                              tm_b, tm_xo, tm_wo, ga)
+                             : launch_cluster(k_gemm_tc<false, true, T, 128>, grid, block, kGemmSmem, s, true, 2u,
+                                              tm_a, tm_b, tm_xo, tm_wo, ga);
+        return write_i32 ? launch_cluster(k_gemm_tc<true, true, T, 256>, grid, block, kGemmSmem, s, true, 2u, tm_a,
+                                          tm_b, tm_xo, tm_wo, ga)
+                         : launch_cluster(k_gemm_tc<false, true, T, 256>, grid, block, kGemmSmem, s, true, 2u, tm_a,
+                                          tm_b, tm_xo, tm_wo, ga);
     }
-    const int ntiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-    const int grid = ntiles < dev->sms ? ntiles : dev->sms;
-    if (write_i32)
-        return launch(k_gemm_tc<true, false, T>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo,
-                      tm_wo, ga);
-    return launch(k_gemm_tc<false, false, T>, dim3(grid), dim3(kGemmThreads), kGemmSmem, s, true, tm_a, tm_b, tm_xo,
-                  tm_wo, ga);
+    const dim3 grid(g.ctas_or_clusters);
+    if (g.bn == 128)
+        return write_i32 ? launch(k_gemm_tc<true, false, T, 128>, grid, block, kGemmSmem, s, true, tm_a, tm_b, tm_xo,
+                                  tm_wo, ga)
+                         : launch(k_gemm_tc<false, false, T, 128>, grid, block, kGemmSmem, s, true, tm_a, tm_b, tm_xo,
+                                  tm_wo, ga);
+    return write_i32 ? launch(k_gemm_tc<true, false, T, 256>, grid, block, kGemmSmem, s, true, tm_a, tm_b, tm_xo,
+                              tm_wo, ga)
+                     : launch(k_gemm_tc<false, false, T, 256>, grid, block, kGemmSmem, s, true, tm_a, tm_b, tm_xo,
+                              tm_wo, ga);
 }
 
 // Kernels one matmul call launches (the plan matmul_impl follows).
@@ -538,10 +559,11 @@ int kernels_per_call(int M, int K, int N, float threshold, bool write_i32) {
     const bool scan = use_outliers && !cluster_flags_apply(M, K, threshold);
     int n = (scan ? 1 : 0) + 1 + 1;  // scan, row quant, GEMV / GEMM
     // outlier rows of W16 for the GEMM, unless the row quantization gathers them
-    if (M > LLMINT8_DECODE_MAX_M && use_outliers && !write_i32 && K > 4096) n += 1;
+    if (M > LLMINT8_DECODE_MAX_M && use_outliers && !write_i32 &&
+        !rowq_gathers_w16(false, M, K, N, threshold, write_i32, reinterpret_cast<const void*>(1)))
+        n += 1;
     // the codes widened to fp16 for the tensor cores
     if (M > LLMINT8_DECODE_MAX_M) n += 1;
-    (void)N;
     return n;
 }
 
@@ -557,7 +579,7 @@ llmint8_status matmul_impl(const void* X, int M, int K, int N, float threshold, 
     if ((st = current_device(&dev)) != LLMINT8_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the row quantization gathers only from a full fp16 copy (W16 is null in w8 mode)
-    const bool gw = !src.w8 && rowq_gathers_w16(L.decode, K, threshold, write_i32, W16);
+    const bool gw = !src.w8 && rowq_gathers_w16(L.decode, M, K, N, threshold, write_i32, W16);
     const void* W16g = src.w8 ? nullptr : W16;
     if (bf16) {
         if ((st = xpass_launch<__nv_bfloat16>(X, M, K, threshold, workspace, L, dev, s, W16, N, gw)) != LLMINT8_OK)

@@ -55,13 +55,15 @@ static_assert(kStages * (kStageA + kStageB) == kPairStages * (kStageA + kPairSta
 constexpr size_t kGemmSmem = 1024 /*align slack*/ + (size_t)kStages * (kStageA + kStageB) + 256;
 
 // Ring depth and B bytes per stage of one CTA for a tile width BN (256, or 128
-// for CTA pairs when wide tiles would leave SMs idle): the rings fill the same
-// 192 KB.
-__host__ __device__ constexpr int gemm_stages(bool pair, int BN) { return !pair ? kStages : BN == 256 ? kPairStages : 8; }
+// when wide tiles would leave SMs idle): the rings fill the same 192 KB.
+__host__ __device__ constexpr int gemm_stages(bool pair, int BN) {
+    return !pair ? (BN == 256 ? kStages : kPairStages) : BN == 256 ? kPairStages : 8;
+}
 __host__ __device__ constexpr uint32_t gemm_stage_b(bool pair, int BN) {
     return (uint32_t)(pair ? BN / 2 : BN) * kBK * 2;
 }
-static_assert(gemm_stages(true, 128) * (kStageA + gemm_stage_b(true, 128)) == kStages * (kStageA + kStageB),
+static_assert(gemm_stages(true, 128) * (kStageA + gemm_stage_b(true, 128)) == kStages * (kStageA + kStageB) &&
+                  gemm_stages(false, 128) * (kStageA + gemm_stage_b(false, 128)) == kStages * (kStageA + kStageB),
               "same ring size");
 
 struct GemmArgs {
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_wo, GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    static_assert(BN == kBN || (PAIR && BN == 128), "tile widths: 256, or 128 for CTA pairs");
+    static_assert(BN == kBN || BN == 128, "tile widths: 256 or 128");
     constexpr int S = gemm_stages(PAIR, BN);
     constexpr uint32_t SB = gemm_stage_b(PAIR, BN);  // B bytes of a stage in this CTA
     constexpr uint32_t TC = 2 * BN;                  // TMEM columns: two fp32 accumulators
@@ -244,10 +246,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const int s_begin = ch < nchunks_int ? ch * kChunkSteps : ksteps;
-                    const int s_end = ch < nchunks_int ? min(ksteps, s_begin + kChunkSteps) : ksteps + osteps;
+                    const bool int_chunk = ch < nchunks_int;
+                    const int s_begin = int_chunk ? ch * kChunkSteps : ksteps;
+                    const int s_end = int_chunk ? min(ksteps, s_begin + kChunkSteps) : ksteps + osteps;
                     const uint32_t d_tmem = tmem_base + b * (uint32_t)BN;
-                    const uint32_t id = ch < nchunks_int ? idesc : idesc_o;
+                    const uint32_t id = int_chunk ? idesc : idesc_o;
                     for (int s = s_begin; s < s_end; ++s) {
                         if (!wait_bar(&ss->full[stage], phase)) {
                             fail(3);

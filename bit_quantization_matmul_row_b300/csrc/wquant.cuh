@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kWidenThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kWidenIn; ++i) mbar_init(&full[i], 1);
         fence_mbar_init();
+        s_ok = 1u;
     }
     __syncthreads();
     pdl_trigger();

@@ -395,9 +395,10 @@ llmint8_status llmint8_gemm_i32(const int8_t *Xq, const int8_t *Wq, int M, int K
  * for llmint8_matmul_int8): the outlier scan (not run at +INFINITY, nor for
  * M <= 16 with K <= 4096, where the row-quantization CTAs form one cluster and
  * find the outlier columns themselves), the row quantization, for M > 16 with a
- * finite threshold, write_i32 = 0 and K > 4096 the gather of the outlier rows
- * of W16 (for K <= 4096 the row quantization writes them), for M > 16 the
- * widening of the weight codes to fp16, and the GEMV or GEMM.
+ * finite threshold and write_i32 = 0 the gather of the outlier rows of W16
+ * (unless the row quantization writes them: K <= 4096 and ceil(M/8) * 8 >=
+ * N/16), for M > 16 the widening of the weight codes to fp16, and the GEMV or
+ * GEMM.
  * The bf16 entry points launch the same kernels; llmint8_matmul_w8 launches the
  * gather for every M > 16 with a finite threshold (one more kernel when
  * K <= 4096).  -1 for arguments the call would reject as EINVAL.

@@ -214,9 +214,12 @@ def test_kernels_per_call(lib):
         assert k(M, K, 4096, 6.0, 0) == 3, (M, K)
         assert k(M, K, 4096, inf, 0) == 2       # no outlier scan
     # prefill: scan + row quantization (which also gathers the outlier rows of W16
-    # when rows have at most 4096 columns) + widening of the codes + GEMM
-    assert k(17, 4096, 4096, 6.0, 0) == 4
-    assert k(17, 4112, 4096, 6.0, 0) == 5       # separate gather of the outlier rows of W16
+    # when rows have at most 4096 columns and its M/8 CTAs cover the N/16 column
+    # groups 8 at a time) + widening of the codes + GEMM
+    assert k(2048, 4096, 4096, 6.0, 0) == 4
+    assert k(2048, 4096, 11008, 6.0, 0) == 4
+    assert k(17, 4096, 4096, 6.0, 0) == 5       # 3 row CTAs: separate gather of the outlier rows of W16
+    assert k(17, 4112, 4096, 6.0, 0) == 5       # rows too long for the fused gather
     assert k(17, 4096, 4096, 6.0, 1) == 4       # the int32 result leaves out the fp16 slice
     assert k(17, 4096, 4096, inf, 0) == 3
     assert k(0, 64, 64, 6.0, 0) == -1

@@ -86,10 +86,12 @@ def test_decode_outlier_chunks(M, frac):
     assert 256 < len(g["outliers"]) < 512
 
 
-@pytest.mark.parametrize("M,K,N", [(17, 64, 256), (130, 272, 272), (300, 1088, 400), (256, 2112, 512)])
+@pytest.mark.parametrize("M,K,N", [(17, 64, 256), (130, 272, 272), (300, 1088, 400), (256, 2112, 512),
+                                   (100, 4160, 384), (200, 3136, 1040), (64, 1024, 4096)])
 def test_prefill_ragged(M, K, N):
     # ragged M tiles, ragged N tiles (N % 256 != 0), K not a multiple of 64,
-    # K crossing the 1024-long exact chunk boundary
+    # K crossing the 1024-long exact chunk boundary; the last three: medium M on
+    # 128-wide one-CTA and pair tiles over several exact chunks
     X, W = xw(M, K, N, frac=0.02, seed=M + K + N, min_count=2)
     check(X, W, 6.0)
 
