@@ -108,11 +108,24 @@ def test_call_with_a_state_from_the_oracle(M, K, N, frac):
     X, _ = synthetic.make_x(M, K, frac=frac, min_count=0 if frac == 0 else 3, seed=M * 7 + K)
     W, Wd, Wq, sw = _weights(K, N, seed=K * 3 + N)
     S_in = _state_from_oracle(X, 6.0)
-    Y = api.llmint8_matmul_chain(torch.from_numpy(X).cuda(), float("nan"), S_in, Wq, sw, Wd)
+    Xg = torch.from_numpy(X).cuda()
+    ws = api.make_workspace(M, K, N, Xg.device)
+    C = torch.empty((M, N), dtype=torch.int32, device=Xg.device)
+    Y = api.llmint8_matmul_chain(Xg, float("nan"), S_in, Wq, sw, Wd, workspace=ws, C=C)
     torch.cuda.synchronize()
     ref = oracle.llmint8_matmul(X, W, 6.0)
     ok, ratio = y_close(Y.cpu().numpy(), ref["Y"])
     assert ok, f"worst error/tolerance {ratio:.3g}"
+    # the kernel rebuilt A1 and A2 from the state: outlier set, row scales and codes
+    # bit for bit, and the exact int32 product of those codes
+    is_out = oracle.outlier_columns(X, 6.0)
+    Xq_ref, sx_ref = oracle.quantize_rows(X, is_out)
+    inter = api.read_intermediates(ws, M, K, N)
+    assert np.array_equal(inter["outliers"].cpu().numpy(), oracle.outlier_indices(is_out)), "outlier set"
+    assert np.array_equal(inter["row_scale"].cpu().numpy().view(np.uint32), sx_ref.view(np.uint32)), "row scales"
+    assert np.array_equal(inter["codes"].cpu().numpy(), Xq_ref), "codes"
+    Wq_ref, _ = oracle.quantize_weight(W)
+    assert np.array_equal(C.cpu().numpy().astype(np.int64), oracle.int8_matmul(Xq_ref, Wq_ref)), "int32 product"
 
 
 @pytest.mark.parametrize("M", [1, 4])
