@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 1u;
         record_error(a.err, kStatusTimeout, where);
     };
-    // whole-warp bounded wait: lane 0 polls, the verdict is broadcast, and the
+    // whole-warp bounded wait: lane 0 polls, the result is broadcast, and the
     // warp is converged again for the .sync.aligned TMEM loads that follow
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         uint32_t got = 0;
