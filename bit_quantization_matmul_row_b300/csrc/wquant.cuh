@@ -93,17 +93,21 @@ __global__ void __launch_bounds__(256) k_quantize_weight_tile(const __half* __re
 // for the weight codes Wq [N, K] and, by llmint8_gemm_i32, for caller codes of X.
 //
 // A bandwidth pass that keeps the load/store path of the SMs out of the way:
-// bulk copies (TMA engine) bring 32 KB slices of the codes into a ring of
-// kWidenIn shared-memory buffers, the CTA widens a slice into one of
-// kWidenOut output buffers (shared memory only), and a bulk store writes it
-// back.  One CTA per SM, grid-strided over slices.  The codes may be read
-// before the predecessor finishes only when they are constant (weights); the
-// scratch is written only after it (the previous call's GEMM may still read
-// it).  Waits are bounded: a timeout records the error word and the CTA stops
-// after letting its copies in flight finish.
-constexpr uint32_t kWidenChunk = 32768;  // int8 bytes per slice (one fence and barrier pair each)
-constexpr int kWidenIn = 3, kWidenOut = 2, kWidenThreads = 256;
-constexpr size_t kWidenSmem = 1024 + (size_t)kWidenIn * kWidenChunk + (size_t)kWidenOut * 2 * kWidenChunk + 256;
+// bulk copies (TMA engine) bring 16 KB slices of the codes into shared memory,
+// they are widened there into an output buffer, and a bulk store writes that
+// back.  One CTA per SM, grid-strided over slices; the CTA runs two independent
+// groups of four warps, each with its own ring of kWidenIn input and kWidenOut
+// output buffers and its own named barrier, taking the CTA's slices in turn, so
+// that one group widens while the other waits for data, fences or stores.  The
+// codes may be read before the predecessor finishes only when they are
+// constant (weights); the scratch is written only after it (the previous
+// call's GEMM may still read it).  Waits are bounded: a timeout records the
+// error word and the group stops after letting its copies in flight finish.
+constexpr uint32_t kWidenChunk = 16384;  // int8 bytes per slice
+constexpr int kWidenGroups = 2, kWidenIn = 3, kWidenOut = 2, kWidenThreads = 256;
+constexpr int kWidenGroupThreads = kWidenThreads / kWidenGroups;
+constexpr size_t kWidenGroupBytes = (size_t)kWidenIn * kWidenChunk + (size_t)kWidenOut * 2 * kWidenChunk;
+constexpr size_t kWidenSmem = 1024 + kWidenGroups * kWidenGroupBytes + 256;
 static_assert(kWidenSmem <= 232448, "one CTA per SM within the opt-in shared memory limit");
 
 __global__ void __launch_bounds__(kWidenThreads, 1)
@@ -111,51 +115,55 @@ __global__ void __launch_bounds__(kWidenThreads, 1)
                   WsHeader* err, uint32_t spin_limit) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* in = sm;                                                // [kWidenIn][kWidenChunk]
-    uint8_t* out = sm + (size_t)kWidenIn * kWidenChunk;              // [kWidenOut][2 * kWidenChunk]
-    uint64_t* full = reinterpret_cast<uint64_t*>(out + (size_t)kWidenOut * 2 * kWidenChunk);  // [kWidenIn]
-    __shared__ uint32_t s_ok;
     const int tid = threadIdx.x;
+    const int grp = tid / kWidenGroupThreads, gtid = tid % kWidenGroupThreads;
+    uint8_t* in = sm + (size_t)grp * kWidenGroupBytes;                // [kWidenIn][kWidenChunk]
+    uint8_t* out = in + (size_t)kWidenIn * kWidenChunk;               // [kWidenOut][2 * kWidenChunk]
+    uint64_t* full_all = reinterpret_cast<uint64_t*>(sm + kWidenGroups * kWidenGroupBytes);
+    uint64_t* full = full_all + grp * kWidenIn;                       // this group's [kWidenIn]
+    __shared__ uint32_t s_ok[kWidenGroups];
     const size_t nchunks = (nbytes + kWidenChunk - 1) / kWidenChunk;
-    auto chunk_of = [&](size_t j) { return (size_t)blockIdx.x + j * gridDim.x; };
+    // the group's slices: the CTA's slices blockIdx.x + i * gridDim.x with i = grp, grp + 2, ...
+    auto chunk_of = [&](size_t j) { return (size_t)blockIdx.x + (j * kWidenGroups + grp) * gridDim.x; };
     auto bytes_of = [&](size_t c) {
         const size_t rest = nbytes - c * kWidenChunk;
         return (uint32_t)(rest < kWidenChunk ? rest : kWidenChunk);
     };
-    auto issue = [&](size_t j) {  // thread 0: slice j of this CTA into ring slot j % kWidenIn
+    auto issue = [&](size_t j) {  // group leader: slice j of the group into ring slot j % kWidenIn
         const size_t c = chunk_of(j);
         if (c >= nchunks) return;
         uint64_t* bar = &full[j % kWidenIn];
         mbar_arrive_expect_tx(bar, bytes_of(c));
         bulk_load_1d(in + (j % kWidenIn) * kWidenChunk, src + c * kWidenChunk, bytes_of(c), bar);
     };
+    auto group_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kWidenGroupThreads) : "memory"); };
     if (tid == 0) {
-        for (int i = 0; i < kWidenIn; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < kWidenGroups * kWidenIn; ++i) mbar_init(&full_all[i], 1);
         fence_mbar_init();
-        s_ok = 1u;
+        for (int g = 0; g < kWidenGroups; ++g) s_ok[g] = 1u;
     }
     __syncthreads();
     pdl_trigger();
     if (!src_constant) pdl_wait();
-    if (tid == 0)
+    if (gtid == 0)
         for (int i = 0; i < kWidenIn; ++i) issue(i);
     pdl_wait();
     size_t j = 0;
     for (; chunk_of(j) < nchunks; ++j) {
         const size_t c = chunk_of(j);
         const int si = (int)(j % kWidenIn), so = (int)(j % kWidenOut);
-        if (tid == 0) {
+        if (gtid == 0) {
             // the output slot's previous bulk store has finished reading it
             if (j >= (size_t)kWidenOut) bulk_wait_read<kWidenOut - 1>();
-            s_ok = mbar_wait_bounded(&full[si], (uint32_t)(j / kWidenIn) & 1u, spin_limit, nullptr) ? 1u : 0u;
+            s_ok[grp] = mbar_wait_bounded(&full[si], (uint32_t)(j / kWidenIn) & 1u, spin_limit, nullptr) ? 1u : 0u;
         }
-        __syncthreads();
-        if (!s_ok) break;
+        group_sync();
+        if (!s_ok[grp]) break;
         const uint32_t nb = bytes_of(c);
         const uint8_t* a = in + (size_t)si * kWidenChunk;
         uint8_t* o = out + (size_t)so * 2 * kWidenChunk;
 #pragma unroll 4
-        for (uint32_t p = tid * 16; p < nb; p += kWidenThreads * 16) {
+        for (uint32_t p = gtid * 16; p < nb; p += kWidenGroupThreads * 16) {
             const uint4 v = *reinterpret_cast<const uint4*>(a + p);
             uint32_t h[8];
             s8x4_to_half2x2(v.x, h[0], h[1]);
@@ -166,15 +174,15 @@ __global__ void __launch_bounds__(kWidenThreads, 1)
             *reinterpret_cast<uint4*>(o + 2 * p + 16) = make_uint4(h[4], h[5], h[6], h[7]);
         }
         fence_proxy_async_smem();  // the bulk store reads these writes through the async proxy
-        __syncthreads();
-        if (tid == 0) {
+        group_sync();
+        if (gtid == 0) {
             bulk_store_1d(dst + c * kWidenChunk, o, 2 * nb);
             bulk_commit();
-            issue(j + kWidenIn);  // the input slot is free again (all threads passed the barrier)
+            issue(j + kWidenIn);  // the input slot is free again (the group passed the barrier)
         }
     }
-    if (tid == 0) {
-        if (!s_ok) {
+    if (gtid == 0) {
+        if (!s_ok[grp]) {
             record_error(err, kStatusTimeout, 30);
             // let the loads already issued land before shared memory goes away
             for (size_t k = j; k < j + kWidenIn && chunk_of(k) < nchunks; ++k)
