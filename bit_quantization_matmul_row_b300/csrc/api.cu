@@ -87,6 +87,19 @@ llmint8_status encode_fp16_2d(CUtensorMap* map, const void* base, int rows, int 
     return r == CUDA_SUCCESS ? LLMINT8_OK : LLMINT8_ECUDA;
 }
 
+// The GEMM output [rows, cols] row-major with elements of `esize` bytes (2: Y,
+// 4: C) for TMA stores: box of 32 rows x 128 bytes, 128-byte swizzle.
+llmint8_status encode_out_2d(CUtensorMap* map, void* base, int rows, int cols, int esize) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / esize), 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base,
+                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? LLMINT8_OK : LLMINT8_ECUDA;
+}
+
 // 2D int8 tensor [rows, cols] row-major (pitch = cols bytes); box of box_rows x
 // box_cols bytes, no swizzle (rows land box_cols bytes apart in shared memory).
 llmint8_status encode_u8_2d(CUtensorMap* map, const void* base, int rows, int cols, int box_rows, int box_cols) {
@@ -493,11 +506,12 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
     // A3 operand: the int8 codes widened to exact fp16 integers in the scratch
     if ((st = widen_launch(Wq, w.wq16, (size_t)N * K, true, w.hdr, dev, s, true)) != LLMINT8_OK) return st;
     if ((st = get_encoder()) != LLMINT8_OK) return st;
-    CUtensorMap tm_a, tm_b, tm_xo, tm_wo;
+    CUtensorMap tm_a, tm_b, tm_xo, tm_wo, tm_out;
     if ((st = encode_fp16_2d(&tm_a, w.codes, M, K, K, kBM)) != LLMINT8_OK) return st;
     if ((st = encode_fp16_2d(&tm_b, w.wq16, N, K, K, b_rows)) != LLMINT8_OK) return st;
     if ((st = encode_fp16_2d(&tm_xo, w.xo, M, L.kp, L.kp, kBM)) != LLMINT8_OK) return st;
     if ((st = encode_fp16_2d(&tm_wo, w.w16o, N, L.kp, L.kp, b_rows)) != LLMINT8_OK) return st;
+    if ((st = encode_out_2d(&tm_out, out, M, N, write_i32 ? 4 : 2)) != LLMINT8_OK) return st;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!dev->gemm_attr_set[Fmt<T>::kBF16]) {
@@ -519,7 +533,6 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
     ga.col_scale = colScaleW;
     ga.hdr = w.hdr;
     ga.err = w.hdr;
-    ga.out = out;
     ga.M = M;
     ga.N = N;
     ga.K = K;
@@ -531,24 +544,24 @@ llmint8_status gemm_launch(const void* X, int M, int K, int N, float threshold, 
         const dim3 grid(2 * g.ctas_or_clusters);
         if (g.bn == 128)
             return write_i32 ? launch_cluster(k_gemm_tc<true, true, T, 128>, grid, block, kGemmSmem, s, true, 2u, tm_a,
-                                              tm_b, tm_xo, tm_wo, ga)
+                                              tm_b, tm_xo, tm_wo, tm_out, ga)
                              : launch_cluster(k_gemm_tc<false, true, T, 128>, grid, block, kGemmSmem, s, true, 2u,
-                                              tm_a, tm_b, tm_xo, tm_wo, ga);
+                                              tm_a, tm_b, tm_xo, tm_wo, tm_out, ga);
         return write_i32 ? launch_cluster(k_gemm_tc<true, true, T, 256>, grid, block, kGemmSmem, s, true, 2u, tm_a,
-                                          tm_b, tm_xo, tm_wo, ga)
+                                          tm_b, tm_xo, tm_wo, tm_out, ga)
                          : launch_cluster(k_gemm_tc<false, true, T, 256>, grid, block, kGemmSmem, s, true, 2u, tm_a,
-                                          tm_b, tm_xo, tm_wo, ga);
+                                          tm_b, tm_xo, tm_wo, tm_out, ga);
     }
     const dim3 grid(g.ctas_or_clusters);
     if (g.bn == 128)
         return write_i32 ? launch(k_gemm_tc<true, false, T, 128>, grid, block, kGemmSmem, s, true, tm_a, tm_b, tm_xo,
-                                  tm_wo, ga)
+                                  tm_wo, tm_out, ga)
                          : launch(k_gemm_tc<false, false, T, 128>, grid, block, kGemmSmem, s, true, tm_a, tm_b, tm_xo,
-                                  tm_wo, ga);
+                                  tm_wo, tm_out, ga);
     return write_i32 ? launch(k_gemm_tc<true, false, T, 256>, grid, block, kGemmSmem, s, true, tm_a, tm_b, tm_xo,
-                              tm_wo, ga)
+                              tm_wo, tm_out, ga)
                      : launch(k_gemm_tc<false, false, T, 256>, grid, block, kGemmSmem, s, true, tm_a, tm_b, tm_xo,
-                              tm_wo, ga);
+                              tm_wo, tm_out, ga);
 }
 
 // Kernels one matmul call launches (the plan matmul_impl follows).

@@ -258,6 +258,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* desc, ui
         : "memory");
 }
 
+// 2D tiled store of a shared-memory box (laid out as the tensor map's swizzle
+// says) to global memory; completes in this thread's current bulk group.
+// Elements of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void* desc, const void* smem_src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(desc),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // ----------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor core, TMEM accumulators)
 // ----------------------------------------------------------------------------

@@ -14,12 +14,18 @@
 // The fp16 outlier slice (A4: X[:, O] . W16[O, :], fp32 accumulate) is one more
 // chunk of the same pipeline, fed from the gathered operands Xo [M, Kp] and
 // W16oT [N, Kp]; it stays in fp32.  The epilogue then computes
-// Y = fp16(C * s_x[i] * s_w[n] / 127^2 + F) and stores it (A5).
+// Y = fp16(C * s_x[i] * s_w[n] / 127^2 + F) (A5) into registers, frees the
+// TMEM buffer at once (the tensor core is already on the next tile and needs
+// it one chunk later), and writes Y through a shared-memory staging buffer
+// with TMA tensor stores: whole 128-byte row segments instead of one 16-byte
+// piece per thread and row, which had flooded the L2 with partial-sector
+// writes and slowed the operand loads of the next tile.
 //
 // Roles (320 threads, one CTA per SM, persistent over 128 x 256 output tiles):
 //   warp 0      TMA producer: 4-stage ring of (A 128x64, B 256x64) fp16 tiles
 //   warp 1      TMEM owner and MMA issuer (one thread), M=128 N=256 K=16 MMAs
-//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).., column half (w-2)/4
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4).., column half (w-2)/4,
+//               and stores its 32 rows through its own 4 KB staging buffer
 //
 // PAIR (M > 128): the CTAs run as clusters of two that compute 256 x 256 tiles
 // with tcgen05.mma.cta_group::2.  Each CTA loads its own 128 rows of A and its
@@ -52,7 +58,13 @@ constexpr uint32_t kStageB = kBN * kBK * 2;  // 32 KB
 constexpr uint32_t kPairStageB = kStageB / 2;  // 16 KB: the CTA's half of the B tile
 constexpr uint32_t kTmemCols = 512;          // two 256-column fp32 accumulators
 static_assert(kStages * (kStageA + kStageB) == kPairStages * (kStageA + kPairStageB), "same ring size");
-constexpr size_t kGemmSmem = 1024 /*align slack*/ + (size_t)kStages * (kStageA + kStageB) + 256;
+// After the ring: the barriers (1 KB block), then one output staging buffer per
+// epilogue warp: 32 rows x 128 bytes, the box of a TMA store with the 128-byte
+// swizzle (64 fp16 or 32 int32 columns of the warp's 32 rows).
+constexpr uint32_t kOutStage = 32 * 128;
+constexpr size_t kGemmSmem =
+    1024 /*align slack*/ + (size_t)kStages * (kStageA + kStageB) + 1024 + (size_t)kEpiWarps * kOutStage;
+static_assert(kGemmSmem <= 232448, "shared memory of one CTA");
 
 // Ring depth and B bytes per stage of one CTA for a tile width BN (256, or 128
 // when wide tiles would leave SMs idle): the rings fill the same 192 KB.
@@ -71,7 +83,6 @@ struct GemmArgs {
     const float* col_scale;  // [N]
     const WsHeader* hdr;     // outlier_count
     WsHeader* err;           // error word
-    void* out;               // Y fp16 [M, N] or C int32 [M, N]
     int M, N, K;
     int use_outliers;
     uint32_t spin_limit;
@@ -90,7 +101,8 @@ struct GemmSmem {
 template <bool WRITE_I32, bool PAIR, typename T, int BN = kBN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-              const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_wo, GemmArgs a) {
+              const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_wo,
+              const __grid_constant__ CUtensorMap tm_out, GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     static_assert(BN == kBN || BN == 128, "tile widths: 256 or 128");
@@ -101,6 +113,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* stage_a = smem;
     uint8_t* stage_b = smem + S * kStageA;
     GemmSmem* ss = reinterpret_cast<GemmSmem*>(smem + S * (kStageA + SB));
+    static_assert(sizeof(GemmSmem) <= 1024, "barrier block");
+    uint8_t* stage_out = smem + S * (kStageA + SB) + 1024;  // 1024-aligned, as the swizzle needs
     volatile uint32_t* abort_flag = &ss->abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -134,6 +148,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(&tm_out);
         if (a.use_outliers) {
             tma_prefetch_desc(&tm_xo);
             tma_prefetch_desc(&tm_wo);
@@ -305,13 +320,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             else
                 mbar_arrive(&ss->tmem_empty[b]);
         };
+        // This warp's output staging buffer.  At the start of a tile its first
+        // HC floats receive the column scales of the warp's columns; once the
+        // values of the tile are in registers it receives one TMA box of output
+        // at a time: row r (= lane) as eight 16-byte chunks, chunk k at position
+        // k ^ (r % 8) (the 128-byte swizzle).
+        uint8_t* stg = stage_out + ew * kOutStage;
+        const float* cs = reinterpret_cast<const float*>(stg);
+        auto stage_row = [&](int k, uint4 v) {
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) = v;
+        };
+        // publish the staged box to the async proxy and store it; the next
+        // writer of the buffer waits for the store to have read it
+        auto store_box = [&](int x, int y0) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && x < a.N && y0 < a.M) {
+                tma_store_2d(&tm_out, stg, x, y0);
+                bulk_commit();
+            }
+        };
+        auto buffer_free = [&]() {
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+        };
         for (int tile = unit0; tile < ntiles && ok; tile += ustride) {
             const int tm = tile % tiles_m, tn = tile / tiles_m;
-            const int row = row_of(tm) + q * 32 + lane;
+            const int row0 = row_of(tm) + q * 32;  // first of this warp's 32 rows
+            const int row = row0 + lane;
             const int col0 = tn * BN + h * HC;
-            int32_t sum[HC];
+            buffer_free();
+            if constexpr (!WRITE_I32) {
+                // read once per tile, while the tensor core works on the first
+                // chunk (N is a multiple of 16: whole float4s)
+                float* csw = reinterpret_cast<float*>(stg);
+                for (int c = lane * 4; c < HC; c += 128) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (col0 + c < a.N) v = __ldg(reinterpret_cast<const float4*>(a.col_scale + col0 + c));
+                    *reinterpret_cast<float4*>(csw + c) = v;
+                }
+                __syncwarp();
+            }
+            // Exact conversion of a chunk's integer-valued fp32 sums v: for |v| <=
+            // 2^22, v + 1.5 * 2^23 is a float of exponent 23 whose bit pattern is
+            // 0x4B400000 + v.  The int32 sum adds these patterns and starts from
+            // -nchunks * 0x4B400000 (mod 2^32), which leaves the exact integer.  A
+            // batch of 16 in which some |v| reaches 2^22 (possible only close to the
+            // 2^24 bound of a chunk) is converted by cvt.rni instead, for the whole warp.
+            uint32_t sum[HC];
+            const uint32_t bias = 0u - (uint32_t)nchunks_int * 0x4B400000u;
 #pragma unroll
-            for (int c = 0; c < HC; ++c) sum[c] = 0;
+            for (int c = 0; c < HC; ++c) sum[c] = bias;
             for (int ch = 0; ch < nchunks_int; ++ch, ++chunk) {
                 const uint32_t b = chunk & 1u, use = (chunk >> 1) & 1u;
                 const bool got = warp_wait(&ss->tmem_full[b], use);
@@ -326,8 +385,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t r[16];
                     tmem_ld_32x32b_x16(tmem_base + lane_base + b * BN + h * HC + j * 16, r);
                     tmem_ld_wait();
+                    float mx = 0.f;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) sum[j * 16 + c] += __float2int_rn(__uint_as_float(r[c]));
+                    for (int c = 0; c < 16; ++c) mx = fmaxf(mx, fabsf(__uint_as_float(r[c])));
+                    if (__any_sync(0xffffffffu, mx >= 4194304.0f)) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            sum[j * 16 + c] += (uint32_t)__float2int_rn(__uint_as_float(r[c])) + 0x4B400000u;
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            sum[j * 16 + c] += __float_as_uint(__fadd_rn(__uint_as_float(r[c]), 12582912.0f));
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -346,59 +415,68 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 tc_fence_after();
             }
-            const bool row_ok = row < a.M;
-            const float sx = row_ok ? __ldcg(a.row_scale + row) * (1.0f / 16129.0f) : 0.0f;
-#pragma unroll
-            for (int j = 0; j < HC / 16; ++j) {
-                uint32_t r[16];
+            // the fp32 accumulator is released as soon as its values are in
+            // registers; the stores of the tile follow
+            auto release_final = [&]() {
                 if (has_f) {
-                    tmem_ld_32x32b_x16(tmem_base + lane_base + fb * BN + h * HC + j * 16, r);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) r[c] = 0u;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) release(fb);
+                    ++chunk;
                 }
-                const int cb = col0 + j * 16;
-                if (row_ok) {
-                    if (WRITE_I32) {
-                        int32_t* orow = reinterpret_cast<int32_t*>(a.out) + (size_t)row * a.N;
+            };
+            if constexpr (WRITE_I32) {
+                release_final();  // C alone: the outlier chunk is not run for int32 output
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            if (cb + v * 4 < a.N)
-                                *reinterpret_cast<int4*>(orow + cb + v * 4) =
-                                    make_int4(sum[j * 16 + v * 4], sum[j * 16 + v * 4 + 1], sum[j * 16 + v * 4 + 2],
-                                              sum[j * 16 + v * 4 + 3]);
+                for (int p = 0; p < HC / 32; ++p) {  // boxes of 32 int32 columns
+                    if (p > 0) buffer_free();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        stage_row(k, make_uint4(sum[p * 32 + k * 4], sum[p * 32 + k * 4 + 1], sum[p * 32 + k * 4 + 2],
+                                                sum[p * 32 + k * 4 + 3]));
+                    store_box(col0 + p * 32, row0);
+                }
+            } else {
+                const float sx = row < a.M ? __ldcg(a.row_scale + row) * (1.0f / 16129.0f) : 0.0f;
+                uint32_t o[HC / 2];  // Y values, two per word
+#pragma unroll
+                for (int j = 0; j < HC / 16; ++j) {
+                    uint32_t r[16];
+                    if (has_f) {
+                        tmem_ld_32x32b_x16(tmem_base + lane_base + fb * BN + h * HC + j * 16, r);
+                        tmem_ld_wait();
                     } else {
-                        uint16_t* orow = reinterpret_cast<uint16_t*>(a.out) + (size_t)row * a.N;
 #pragma unroll
-                        for (int v = 0; v < 2; ++v) {
-                            const int c8 = cb + v * 8;
-                            if (c8 < a.N) {
-                                const float4 s0 = __ldg(reinterpret_cast<const float4*>(a.col_scale + c8));
-                                const float4 s1 = __ldg(reinterpret_cast<const float4*>(a.col_scale + c8 + 4));
-                                const float sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-                                uint32_t o[4];
+                        for (int c = 0; c < 16; ++c) r[c] = 0u;
+                    }
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int c = v * 8 + 2 * e;
-                                    const float y0 = fmaf((float)sum[j * 16 + c], sx * sw[2 * e], __uint_as_float(r[c]));
-                                    const float y1 =
-                                        fmaf((float)sum[j * 16 + c + 1], sx * sw[2 * e + 1], __uint_as_float(r[c + 1]));
-                                    o[e] = Fmt<T>::pack2(y0, y1);
-                                }
-                                *reinterpret_cast<uint4*>(orow + c8) = make_uint4(o[0], o[1], o[2], o[3]);
-                            }
-                        }
+                    for (int v = 0; v < 4; ++v) {
+                        const float4 s4 = *reinterpret_cast<const float4*>(cs + j * 16 + v * 4);
+                        const int c = j * 16 + v * 4;
+                        const float y0 = fmaf((float)(int32_t)sum[c], sx * s4.x, __uint_as_float(r[v * 4]));
+                        const float y1 = fmaf((float)(int32_t)sum[c + 1], sx * s4.y, __uint_as_float(r[v * 4 + 1]));
+                        const float y2 = fmaf((float)(int32_t)sum[c + 2], sx * s4.z, __uint_as_float(r[v * 4 + 2]));
+                        const float y3 = fmaf((float)(int32_t)sum[c + 3], sx * s4.w, __uint_as_float(r[v * 4 + 3]));
+                        o[c / 2] = Fmt<T>::pack2(y0, y1);
+                        o[c / 2 + 1] = Fmt<T>::pack2(y2, y3);
                     }
                 }
-            }
-            if (has_f) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) release(fb);
-                ++chunk;
+                release_final();
+                __syncwarp();  // every lane has read the column scales
+#pragma unroll
+                for (int p = 0; p < HC / 64; ++p) {  // boxes of 64 fp16 columns
+                    if (p > 0) buffer_free();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        stage_row(k, make_uint4(o[p * 32 + k * 4], o[p * 32 + k * 4 + 1], o[p * 32 + k * 4 + 2],
+                                                o[p * 32 + k * 4 + 3]));
+                    store_box(col0 + p * 64, row0);
+                }
             }
         }
+        // stores in flight complete before the CTA exits
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
