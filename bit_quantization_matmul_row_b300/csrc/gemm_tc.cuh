@@ -6,10 +6,10 @@
 // tcgen05.mma kind::f16 as exact fp16 integers.  Each product is an integer of
 // magnitude <= 127^2 = 16129 and each partial sum over at most 1024 products
 // stays below 2^24, so the fp32 TMEM accumulator holds it exactly.  The K loop
-// is cut into chunks of 1024 (16 steps of 64); each chunk is accumulated into
-// one of two TMEM buffers and the epilogue warps drain it into int32 registers
-// while the tensor core fills the other buffer.  The integer product C is thus
-// exact for any K (A3).
+// is cut into chunks of at most 1024 (16 steps of 64) and equal length; each
+// chunk is accumulated into one of two TMEM buffers and the epilogue warps
+// drain it into int32 registers while the tensor core fills the other buffer.
+// The integer product C is thus exact for any K (A3).
 //
 // The fp16 outlier slice (A4: X[:, O] . W16[O, :], fp32 accumulate) is one more
 // chunk of the same pipeline, fed from the gathered operands Xo [M, Kp] and
@@ -261,9 +261,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    // the K steps in nchunks_int chunks of equal length (+-1, at most
+                    // 16): no short tail chunk whose drain outlasts its MMAs
                     const bool int_chunk = ch < nchunks_int;
-                    const int s_begin = int_chunk ? ch * kChunkSteps : ksteps;
-                    const int s_end = int_chunk ? min(ksteps, s_begin + kChunkSteps) : ksteps + osteps;
+                    const int s_begin = int_chunk ? ch * ksteps / nchunks_int : ksteps;
+                    const int s_end = int_chunk ? (ch + 1) * ksteps / nchunks_int : ksteps + osteps;
                     const uint32_t d_tmem = tmem_base + b * (uint32_t)BN;
                     const uint32_t id = int_chunk ? idesc : idesc_o;
                     for (int s = s_begin; s < s_end; ++s) {
