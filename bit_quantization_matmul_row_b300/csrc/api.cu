@@ -362,7 +362,10 @@ llmint8_status xpass_launch(const void* X, int M, int K, float threshold, void* 
     ra.w16o = gather_w16 ? w.w16o : nullptr;
     ra.w16o_pitch = L.kp;
     if (!L.decode && K <= 4096) {  // many short rows: one warp per row
-        const dim3 grid((M + kRowsPerCta - 1) / kRowsPerCta), block(kRowsPerCta * 32);
+        // rows per CTA: as many as spread the rows over two CTAs per SM, at most 8
+        const int per_cta = std::max(1, std::min(kRowsPerCta, (M + 2 * dev->sms - 1) / (2 * dev->sms)));
+        ra.rows_per_cta = per_cta;
+        const dim3 grid((M + per_cta - 1) / per_cta), block(kRowsPerCta * 32);
         if (K <= 1024) return launch(k_row_quant_warp<4, T>, grid, block, 0, s, pdl, ra);
         if (K <= 2048) return launch(k_row_quant_warp<8, T>, grid, block, 0, s, pdl, ra);
         return launch(k_row_quant_warp<16, T>, grid, block, 0, s, pdl, ra);

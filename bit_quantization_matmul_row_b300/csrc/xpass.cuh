@@ -134,6 +134,7 @@ struct RowQuantArgs {
     int w16o_pitch;
     int cluster_flags;        // launched as one cluster of M CTAs: the outlier columns are
                               // found here (no scan kernel, the bit map is not read)
+    int rows_per_cta;         // k_row_quant_warp: rows of a CTA (<= 8; its other warps idle)
 };
 
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -385,7 +386,9 @@ __global__ void __launch_bounds__(kRowThreads) k_row_quant(RowQuantArgs a) {
 }
 
 // A2 for many rows of at most 256 * VPL columns (prefill): one warp per row,
-// 8 rows per CTA.  The CTA reads the outlier bit map and forms its prefix once
+// up to 8 rows per CTA (fewer when that spreads the rows evenly: two CTAs fit
+// on an SM, and 256 CTAs of 8 rows on 148 SMs would give 108 SMs twice the rows
+// of the other 40).  The CTA reads the outlier bit map and forms its prefix once
 // for its 8 rows; each warp holds its row in registers (VPL 16-byte vectors
 // per lane), reduces the masked absmax with shuffles, writes the codes and
 // places its outlier values from the same registers.  No barrier sits between
@@ -410,8 +413,8 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) k_row_quant_warp(RowQuantArg
     __shared__ __align__(16) __half s_tile[64][kGatherCols];  // 64 outliers x 16 columns
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int row = blockIdx.x * kRowsPerCta + warp;
-    const bool live = row < a.M;
+    const int row = blockIdx.x * a.rows_per_cta + warp;
+    const bool live = warp < a.rows_per_cta && row < a.M;
     const int K = a.K;
     const int nwords = (K + 31) >> 5;
     const int nvec = K >> 3;  // K % 16 == 0
